@@ -1,0 +1,484 @@
+// C ABI of the ZVC library: argument checks, sizes, launches, the offload/prefetch
+// pipeline and error readback. Every byte of compressed data is produced and consumed
+// by the kernels in zvc_compress.cu and zvc_decompress.cu; this file only moves
+// pointers, sizes and copies.
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <vector>
+
+#include "zvc_internal.cuh"
+
+using namespace zvc;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+constexpr uint64_t kMaxElems = 1ull << 40;  // keeps every size computation far from overflow
+constexpr int kPipeDepth = 3;               // staging buffers in flight for offload/prefetch
+
+bool chunk_ok(uint32_t c) { return c != 0 && c % kWindow == 0 && c <= ZVC_MAX_CHUNK_ELEMS; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+uint64_t stream_bound(uint64_t n, uint32_t c) {
+  return 32 + 8 * ceil_div_u64(n, c) + 4 * ceil_div_u64(n, kWindow) + 4 * n;
+}
+
+// Smallest valid stream for n words: every mask zero.
+uint64_t stream_floor(uint64_t n, uint32_t c) {
+  return 32 + 8 * ceil_div_u64(n, c) + 4 * ceil_div_u64(n, kWindow);
+}
+
+uint64_t batch_prefix(uint32_t T) { return 16 + 8 * ((uint64_t)T + 1); }
+
+uint64_t compress_ws_bytes(uint64_t total_tiles, uint32_t T) {
+  return round_up_u64(kStatusOffset + 8 * total_tiles + 8 * (uint64_t)T, ZVC_WORKSPACE_ALIGN);
+}
+
+void put_u32(uint8_t* p, uint32_t v) { std::memcpy(p, &v, 4); }
+void put_u64(uint8_t* p, uint64_t v) { std::memcpy(p, &v, 8); }
+uint32_t get_u32(const uint8_t* p) { uint32_t v; std::memcpy(&v, p, 4); return v; }
+uint64_t get_u64(const uint8_t* p) { uint64_t v; std::memcpy(&v, p, 8); return v; }
+
+// ---------------------------------------------------------------- offload plan
+struct SegPlan {
+  uint64_t seg;         // words per segment (whole chunks)
+  uint64_t count;       // segments
+  uint64_t kernel_ws;   // workspace bytes for one segment's compress
+  uint64_t stage;       // bytes of one staging buffer
+  uint64_t sizes_off;   // offset of the per-buffer size slots
+  uint64_t stage_off;   // offset of staging buffer 0
+  uint64_t total;       // workspace bytes
+};
+
+uint64_t segment_elems(uint64_t n, uint32_t c) {
+  // About eight segments per tensor, each between 4 MiB and 64 MiB of words, so the copy
+  // of one segment overlaps the compression of the next; whole chunks only.
+  uint64_t s = ceil_div_u64(n, 8);
+  if (s < (1ull << 20)) s = 1ull << 20;
+  if (s > (1ull << 24)) s = 1ull << 24;
+  return round_up_u64(s, c);
+}
+
+SegPlan seg_plan(uint64_t n, uint32_t c) {
+  SegPlan p;
+  p.seg = segment_elems(n, c);
+  p.count = ceil_div_u64(n, p.seg);
+  const uint64_t seg_n = n < p.seg ? n : p.seg;
+  p.kernel_ws = compress_ws_bytes(tiles_for(seg_n), 1);
+  p.stage = round_up_u64(stream_bound(seg_n, c), ZVC_WORKSPACE_ALIGN);
+  p.sizes_off = p.kernel_ws;
+  p.stage_off = p.sizes_off + ZVC_WORKSPACE_ALIGN;
+  p.total = p.stage_off + kPipeDepth * p.stage;
+  return p;
+}
+
+// Side stream and events for the pipeline, one set per device, created on first use.
+struct Pipe {
+  cudaStream_t side = nullptr;
+  cudaEvent_t kernel_done[kPipeDepth];
+  cudaEvent_t copy_done[kPipeDepth];
+  cudaEvent_t start = nullptr;
+  std::mutex mu;
+};
+
+std::mutex g_pipes_mu;
+std::map<int, Pipe*> g_pipes;
+
+zvc_status get_pipe(Pipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_failure(e);
+  std::lock_guard<std::mutex> lk(g_pipes_mu);
+  auto it = g_pipes.find(dev);
+  if (it != g_pipes.end()) {
+    *out = it->second;
+    return ZVC_OK;
+  }
+  Pipe* p = new Pipe();
+  e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
+  for (int i = 0; i < kPipeDepth && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&p->kernel_done[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done[i], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_failure(e);  // the partial set leaks; CUDA is unusable
+  g_pipes[dev] = p;
+  *out = p;
+  return ZVC_OK;
+}
+
+zvc_status read_latched(void* d_ws) {
+  uint32_t err = 0;
+  cudaError_t e = cudaMemcpy(&err, d_ws, sizeof(err), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_failure(e);
+  return err ? (zvc_status)err : ZVC_ERR_CUDA;
+}
+
+#define ZVC_CUDA_TRY(expr)                          \
+  do {                                              \
+    const cudaError_t e_ = (expr);                  \
+    if (e_ != cudaSuccess) return cuda_failure(e_); \
+  } while (0)
+
+// ---------------------------------------------------------------- tracing
+struct TraceRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+void recycle_trace() {
+  for (const TraceRec& r : g_trace) {
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_trace.clear();
+}
+
+}  // namespace
+
+TraceMark zvc::trace_begin(int kind, cudaStream_t stream) {
+  TraceMark m;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on) return m;
+  TraceRec r{kind, pooled_event(), pooled_event()};
+  if (r.start == nullptr || r.stop == nullptr) return m;
+  cudaEventRecord(r.start, stream);
+  g_trace.push_back(r);
+  m.stop = r.stop;
+  return m;
+}
+
+void zvc::trace_end(TraceMark m, cudaStream_t stream) {
+  if (m.stop != nullptr) cudaEventRecord(m.stop, stream);
+}
+
+zvc_status zvc::cuda_failure(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return ZVC_ERR_CUDA;
+}
+
+extern "C" {
+
+uint64_t zvc_size_bound(uint64_t n, uint32_t chunk_elems) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems) return 0;
+  return stream_bound(n, chunk_elems);
+}
+
+uint64_t zvc_batch_size_bound(const uint64_t* ns, uint32_t T, uint32_t chunk_elems) {
+  if (!chunk_ok(chunk_elems) || T > ZVC_MAX_BATCH || (T > 0 && ns == nullptr)) return 0;
+  uint64_t s = batch_prefix(T);
+  for (uint32_t i = 0; i < T; ++i) {
+    if (ns[i] > kMaxElems) return 0;
+    s += stream_bound(ns[i], chunk_elems);
+  }
+  return s;
+}
+
+uint64_t zvc_workspace_size(uint64_t n, uint32_t chunk_elems) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems) return 0;
+  return compress_ws_bytes(tiles_for(n), 1);
+}
+
+uint64_t zvc_batch_workspace_size(const uint64_t* ns, uint32_t T, uint32_t chunk_elems) {
+  if (!chunk_ok(chunk_elems) || T > ZVC_MAX_BATCH || (T > 0 && ns == nullptr)) return 0;
+  uint64_t tiles = 0;
+  for (uint32_t i = 0; i < T; ++i) {
+    if (ns[i] > kMaxElems) return 0;
+    tiles += tiles_for(ns[i]);
+  }
+  return compress_ws_bytes(tiles, T);
+}
+
+zvc_status zvc_compress(const void* d_in, uint64_t n, uint32_t chunk_elems, void* d_out,
+                        uint64_t out_cap, uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
+                        void* stream) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems || d_out == nullptr || d_ws == nullptr ||
+      (n > 0 && d_in == nullptr) || !aligned(d_in, 4) || !aligned(d_out, 4) ||
+      !aligned(d_ws, ZVC_WORKSPACE_ALIGN) || !aligned(d_out_size, 8))
+    return ZVC_ERR_INVALID_ARG;
+  if (out_cap < stream_bound(n, chunk_elems) || ws_bytes < zvc_workspace_size(n, chunk_elems))
+    return ZVC_ERR_BUFFER_TOO_SMALL;
+  const TensorIn t{static_cast<const uint32_t*>(d_in), n};
+  return launch_compress(&t, 1, false, chunk_elems, static_cast<uint32_t*>(d_out), out_cap / 4,
+                         d_out_size, static_cast<uint8_t*>(d_ws), kDefaultWaitLimitNs,
+                         static_cast<cudaStream_t>(stream));
+}
+
+zvc_status zvc_decompress(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,
+                          uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems || d_in == nullptr || d_ws == nullptr ||
+      (n > 0 && d_out == nullptr) || !aligned(d_in, 4) || !aligned(d_out, 4) ||
+      !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
+    return ZVC_ERR_INVALID_ARG;
+  if (ws_bytes < kControlBytes) return ZVC_ERR_BUFFER_TOO_SMALL;
+  // sizes no valid stream of n words can have
+  if (in_bytes % 4 != 0 || in_bytes < stream_floor(n, chunk_elems) ||
+      in_bytes > stream_bound(n, chunk_elems))
+    return ZVC_ERR_CORRUPT;
+  const TensorOut t{static_cast<uint32_t*>(d_out), n};
+  return launch_decompress(static_cast<const uint32_t*>(d_in), in_bytes, &t, 1, false,
+                           chunk_elems, static_cast<uint8_t*>(d_ws),
+                           static_cast<cudaStream_t>(stream));
+}
+
+zvc_status zvc_compress_batched(const void* const* d_ins, const uint64_t* ns, uint32_t T,
+                                uint32_t chunk_elems, void* d_out, uint64_t out_cap,
+                                uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
+                                void* stream) {
+  if (!chunk_ok(chunk_elems) || T > ZVC_MAX_BATCH || (T > 0 && (d_ins == nullptr || ns == nullptr)) ||
+      d_out == nullptr || d_ws == nullptr || !aligned(d_out, 4) ||
+      !aligned(d_ws, ZVC_WORKSPACE_ALIGN) || !aligned(d_out_size, 8))
+    return ZVC_ERR_INVALID_ARG;
+  std::vector<TensorIn> ts(T);
+  for (uint32_t i = 0; i < T; ++i) {
+    if (ns[i] > kMaxElems || (ns[i] > 0 && d_ins[i] == nullptr) || !aligned(d_ins[i], 4))
+      return ZVC_ERR_INVALID_ARG;
+    ts[i] = TensorIn{static_cast<const uint32_t*>(d_ins[i]), ns[i]};
+  }
+  if (out_cap < zvc_batch_size_bound(ns, T, chunk_elems) ||
+      ws_bytes < zvc_batch_workspace_size(ns, T, chunk_elems))
+    return ZVC_ERR_BUFFER_TOO_SMALL;
+  return launch_compress(ts.data(), T, true, chunk_elems, static_cast<uint32_t*>(d_out),
+                         out_cap / 4, d_out_size, static_cast<uint8_t*>(d_ws),
+                         kDefaultWaitLimitNs, static_cast<cudaStream_t>(stream));
+}
+
+zvc_status zvc_decompress_batched(const void* d_in, uint64_t in_bytes, void* const* d_outs,
+                                  const uint64_t* ns, uint32_t T, uint32_t chunk_elems,
+                                  void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!chunk_ok(chunk_elems) || T > ZVC_MAX_BATCH || (T > 0 && (d_outs == nullptr || ns == nullptr)) ||
+      d_in == nullptr || d_ws == nullptr || !aligned(d_in, 4) || !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
+    return ZVC_ERR_INVALID_ARG;
+  if (ws_bytes < kControlBytes) return ZVC_ERR_BUFFER_TOO_SMALL;
+  std::vector<TensorOut> ts(T);
+  uint64_t floor = batch_prefix(T);
+  for (uint32_t i = 0; i < T; ++i) {
+    if (ns[i] > kMaxElems || (ns[i] > 0 && d_outs[i] == nullptr) || !aligned(d_outs[i], 4))
+      return ZVC_ERR_INVALID_ARG;
+    ts[i] = TensorOut{static_cast<uint32_t*>(d_outs[i]), ns[i]};
+    floor += stream_floor(ns[i], chunk_elems);
+  }
+  if (in_bytes % 4 != 0 || in_bytes < floor || in_bytes > zvc_batch_size_bound(ns, T, chunk_elems))
+    return ZVC_ERR_CORRUPT;
+  return launch_decompress(static_cast<const uint32_t*>(d_in), in_bytes, ts.data(), T, true,
+                           chunk_elems, static_cast<uint8_t*>(d_ws),
+                           static_cast<cudaStream_t>(stream));
+}
+
+uint64_t zvc_offload_segment_elems(uint64_t n, uint32_t chunk_elems) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems) return 0;
+  return segment_elems(n, chunk_elems);
+}
+
+uint64_t zvc_offload_host_bound(uint64_t n, uint32_t chunk_elems) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems) return 0;
+  const SegPlan p = seg_plan(n, chunk_elems);
+  uint64_t s = batch_prefix((uint32_t)p.count);
+  for (uint64_t k = 0; k < p.count; ++k) {
+    const uint64_t nk = (k + 1 < p.count) ? p.seg : n - k * p.seg;
+    s += stream_bound(nk, chunk_elems);
+  }
+  return s;
+}
+
+uint64_t zvc_offload_workspace_size(uint64_t n, uint32_t chunk_elems) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems) return 0;
+  return seg_plan(n, chunk_elems).total;
+}
+
+zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void* h_pinned,
+                       uint64_t h_cap, uint64_t* h_size, void* d_ws, uint64_t ws_bytes,
+                       void* stream) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems || h_pinned == nullptr || h_size == nullptr ||
+      d_ws == nullptr || (n > 0 && d_in == nullptr) || !aligned(d_in, 4) ||
+      !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
+    return ZVC_ERR_INVALID_ARG;
+  const SegPlan p = seg_plan(n, chunk_elems);
+  if (p.count > UINT32_MAX) return ZVC_ERR_INVALID_ARG;
+  if (h_cap < zvc_offload_host_bound(n, chunk_elems) || ws_bytes < p.total)
+    return ZVC_ERR_BUFFER_TOO_SMALL;
+  Pipe* pipe = nullptr;
+  zvc_status st = get_pipe(&pipe);
+  if (st != ZVC_OK) return st;
+  std::lock_guard<std::mutex> lk(pipe->mu);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  uint8_t* H = static_cast<uint8_t*>(h_pinned);
+  uint64_t* dsizes = reinterpret_cast<uint64_t*>(ws + p.sizes_off);
+  const uint32_t* in = static_cast<const uint32_t*>(d_in);
+  const uint64_t S = p.count;
+  const uint64_t prefix = batch_prefix((uint32_t)S);
+  uint64_t pos = prefix;
+  std::vector<uint64_t> offs(S + 1, 0);
+
+  // The compressed size of segment k is copied into its (not yet written) batch-table slot
+  // of the pinned buffer; once the host has seen it, the segment's copy is enqueued.
+  auto enqueue_copy = [&](uint64_t k) -> zvc_status {
+    const int b = (int)(k % kPipeDepth);
+    ZVC_CUDA_TRY(cudaEventSynchronize(pipe->kernel_done[b]));
+    const uint64_t sz = get_u64(H + 16 + 8 * k);
+    if (sz == 0 || sz > p.stage || pos + sz > h_cap) return read_latched(d_ws);
+    offs[k] = pos;
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->kernel_done[b], 0));
+    ZVC_CUDA_TRY(cudaMemcpyAsync(H + pos, ws + p.stage_off + b * p.stage, sz,
+                                 cudaMemcpyDeviceToHost, pipe->side));
+    ZVC_CUDA_TRY(cudaEventRecord(pipe->copy_done[b], pipe->side));
+    pos += sz;
+    return ZVC_OK;
+  };
+
+  for (uint64_t k = 0; k < S; ++k) {
+    const int b = (int)(k % kPipeDepth);
+    if (k >= (uint64_t)kPipeDepth) ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
+    const uint64_t nk = (k + 1 < S) ? p.seg : n - k * p.seg;
+    const TensorIn t{in + k * p.seg, nk};
+    st = launch_compress(&t, 1, false, chunk_elems,
+                         reinterpret_cast<uint32_t*>(ws + p.stage_off + b * p.stage), p.stage / 4,
+                         dsizes + b, ws, kDefaultWaitLimitNs, s);
+    if (st != ZVC_OK) return st;
+    ZVC_CUDA_TRY(cudaMemcpyAsync(H + 16 + 8 * k, dsizes + b, 8, cudaMemcpyDeviceToHost, s));
+    ZVC_CUDA_TRY(cudaEventRecord(pipe->kernel_done[b], s));
+    if (k >= 1 && (st = enqueue_copy(k - 1)) != ZVC_OK) return st;
+  }
+  if (S >= 1 && (st = enqueue_copy(S - 1)) != ZVC_OK) return st;
+  offs[S] = pos;
+
+  put_u32(H + 0, kBatchMagic);
+  put_u32(H + 4, (uint32_t)S);
+  put_u64(H + 8, pos);
+  for (uint64_t k = 0; k <= S; ++k) put_u64(H + 16 + 8 * k, offs[k]);
+  for (uint64_t b = 0; b < S && b < (uint64_t)kPipeDepth; ++b)
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
+  *h_size = pos;
+  return ZVC_OK;
+}
+
+zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint64_t n,
+                        uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems || h_pinned == nullptr || d_ws == nullptr ||
+      (n > 0 && d_out == nullptr) || !aligned(d_out, 4) || !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
+    return ZVC_ERR_INVALID_ARG;
+  const SegPlan p = seg_plan(n, chunk_elems);
+  if (ws_bytes < p.total) return ZVC_ERR_BUFFER_TOO_SMALL;
+  const uint8_t* H = static_cast<const uint8_t*>(h_pinned);
+  const uint64_t S = p.count;
+  const uint64_t prefix = batch_prefix((uint32_t)S);
+  if (h_size < prefix || get_u32(H) != kBatchMagic || get_u32(H + 4) != S ||
+      get_u64(H + 8) != h_size || get_u64(H + 16) != prefix || get_u64(H + 16 + 8 * S) != h_size)
+    return ZVC_ERR_CORRUPT;
+  for (uint64_t k = 0; k < S; ++k) {
+    const uint64_t a = get_u64(H + 16 + 8 * k), b = get_u64(H + 24 + 8 * k);
+    const uint64_t nk = (k + 1 < S) ? p.seg : n - k * p.seg;
+    if (a > b || ((a | b) & 3u) != 0 || b - a < stream_floor(nk, chunk_elems) ||
+        b - a > stream_bound(nk, chunk_elems))
+      return ZVC_ERR_CORRUPT;
+  }
+  Pipe* pipe = nullptr;
+  zvc_status st = get_pipe(&pipe);
+  if (st != ZVC_OK) return st;
+  std::lock_guard<std::mutex> lk(pipe->mu);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  uint32_t* out = static_cast<uint32_t*>(d_out);
+  // copies start after work already enqueued on `stream` (e.g. an offload's copies)
+  ZVC_CUDA_TRY(cudaEventRecord(pipe->start, s));
+  ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->start, 0));
+  for (uint64_t k = 0; k < S; ++k) {
+    const int b = (int)(k % kPipeDepth);
+    const uint64_t a = get_u64(H + 16 + 8 * k), sz = get_u64(H + 24 + 8 * k) - a;
+    uint8_t* stage = ws + p.stage_off + b * p.stage;
+    if (k >= (uint64_t)kPipeDepth) ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->kernel_done[b], 0));
+    ZVC_CUDA_TRY(cudaMemcpyAsync(stage, H + a, sz, cudaMemcpyHostToDevice, pipe->side));
+    ZVC_CUDA_TRY(cudaEventRecord(pipe->copy_done[b], pipe->side));
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
+    const uint64_t nk = (k + 1 < S) ? p.seg : n - k * p.seg;
+    const TensorOut t{out + k * p.seg, nk};
+    st = launch_decompress(reinterpret_cast<const uint32_t*>(stage), sz, &t, 1, false,
+                           chunk_elems, ws, s);
+    if (st != ZVC_OK) return st;
+    ZVC_CUDA_TRY(cudaEventRecord(pipe->kernel_done[b], s));
+  }
+  return ZVC_OK;
+}
+
+zvc_status zvc_get_error(void* d_ws, void* stream) {
+  if (d_ws == nullptr || !aligned(d_ws, ZVC_WORKSPACE_ALIGN)) return ZVC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ZVC_CUDA_TRY(cudaStreamSynchronize(s));
+  uint32_t err = 0;
+  ZVC_CUDA_TRY(cudaMemcpy(&err, d_ws, sizeof(err), cudaMemcpyDeviceToHost));
+  if (err != 0) ZVC_CUDA_TRY(cudaMemset(d_ws, 0, sizeof(Control)));
+  return (zvc_status)err;
+}
+
+zvc_status zvc_selftest_wait_timeout(void* d_ws, uint64_t ws_bytes, uint64_t limit_ns,
+                                     void* stream) {
+  if (d_ws == nullptr || !aligned(d_ws, ZVC_WORKSPACE_ALIGN) || limit_ns == 0 ||
+      limit_ns > kDefaultWaitLimitNs)
+    return ZVC_ERR_INVALID_ARG;
+  if (ws_bytes < compress_ws_bytes(2, 1)) return ZVC_ERR_BUFFER_TOO_SMALL;
+  return launch_lookback_timeout_probe(static_cast<uint8_t*>(d_ws), limit_ns,
+                                       static_cast<cudaStream_t>(stream));
+}
+
+zvc_status zvc_trace_start(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  recycle_trace();
+  g_trace_on = true;
+  return ZVC_OK;
+}
+
+zvc_status zvc_trace_stop(uint64_t* launches, double* device_ms) {
+  if (launches == nullptr || device_ms == nullptr) return ZVC_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = false;
+  for (int k = 0; k < kTraceKinds; ++k) {
+    launches[k] = 0;
+    device_ms[k] = 0.0;
+  }
+  for (const TraceRec& r : g_trace) {
+    ZVC_CUDA_TRY(cudaEventSynchronize(r.stop));
+    float ms = 0.f;
+    ZVC_CUDA_TRY(cudaEventElapsedTime(&ms, r.start, r.stop));
+    launches[r.kind] += 1;
+    device_ms[r.kind] += ms;
+  }
+  recycle_trace();
+  return ZVC_OK;
+}
+
+int zvc_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* zvc_status_string(zvc_status s) {
+  switch (s) {
+    case ZVC_OK: return "ZVC_OK";
+    case ZVC_ERR_INVALID_ARG: return "ZVC_ERR_INVALID_ARG";
+    case ZVC_ERR_BUFFER_TOO_SMALL: return "ZVC_ERR_BUFFER_TOO_SMALL";
+    case ZVC_ERR_CORRUPT: return "ZVC_ERR_CORRUPT";
+    case ZVC_ERR_TIMEOUT: return "ZVC_ERR_TIMEOUT";
+    case ZVC_ERR_CUDA: return "ZVC_ERR_CUDA";
+    default: return "ZVC_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

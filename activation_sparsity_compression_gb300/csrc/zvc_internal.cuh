@@ -1,0 +1,316 @@
+// Internal definitions shared by the ZVC kernels and the C-ABI layer (sm_103a).
+//
+// The stream format is the one documented in include/zvc.h: per 32-word window a 32-bit
+// non-zero mask followed by the non-zero words (Rhu et al., "Compressing DMA Engine",
+// section V.A), grouped into chunks indexed by a u64 offset table behind a 32-byte header.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zvc.h"
+
+namespace zvc {
+
+constexpr uint32_t kWindow = 32;
+constexpr uint32_t kStreamMagic = 0x3143565Au;  // "ZVC1"
+constexpr uint32_t kBatchMagic = 0x4243565Au;   // "ZVCB"
+constexpr uint32_t kVersionWordBytes = 1u | (4u << 16);  // u16 version 1, u16 word_bytes 4
+constexpr uint32_t kStreamHeaderWords = 8;      // 32 bytes
+constexpr uint32_t kBatchHeaderWords = 4;       // 16 bytes
+
+// Workspace layout (device memory owned by the caller, 256-byte aligned).
+//   [0, 256)        Control: latched error, persists across calls until zvc_get_error.
+//   [256, 512)      Counters: finished and failed tile counts, cleared by every call.
+//   [512, ...)      u64 tile_status[tiles], then u64 tensor_start[T], cleared by every call.
+struct Control {
+  uint32_t error;       // first zvc_status latched on the device, 0 if none
+  uint32_t pad;
+  uint64_t error_info;  // tile or chunk index of that error
+};
+struct Counters {
+  unsigned long long unused;
+  unsigned long long done;    // tiles that have published their place
+  unsigned long long failed;  // tiles that gave up
+};
+constexpr uint64_t kControlBytes = 256;
+constexpr uint64_t kCountersBytes = 256;
+constexpr uint64_t kPerCallOffset = kControlBytes;  // counters + status arrays start here
+constexpr uint64_t kStatusOffset = kControlBytes + kCountersBytes;
+
+// Look-back status word: 2-bit flag in bits 63..62, payload word count in bits 61..0.
+constexpr uint64_t kFlagShift = 62;
+constexpr uint64_t kFlagInvalid = 0;    // nothing published yet
+constexpr uint64_t kFlagAggregate = 1;  // value = this tile's own compressed words
+constexpr uint64_t kFlagPrefix = 2;     // value = compressed words of this tile and all before it
+constexpr uint64_t kFlagError = 3;      // this tile gave up; successors give up too
+constexpr uint64_t kValueMask = (1ull << kFlagShift) - 1;
+
+// Compress tiling: one CTA of 256 threads per tile of 4096 words (128 windows); every
+// thread holds 16 words as four 16-byte vectors.
+constexpr int kCompressThreads = 256;
+constexpr int kCompressWarps = kCompressThreads / 32;
+constexpr uint32_t kTileElems = 4096;
+constexpr uint32_t kTileWindows = kTileElems / kWindow;
+
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s per device-side wait
+
+__host__ __device__ inline uint64_t ceil_div_u64(uint64_t a, uint64_t b) {
+  return a / b + (a % b != 0);
+}
+
+inline uint64_t round_up_u64(uint64_t a, uint64_t b) { return ceil_div_u64(a, b) * b; }
+
+inline uint64_t tiles_for(uint64_t n) { return ceil_div_u64(n, kTileElems); }
+
+// Bytes of the per-call region (counters + tile status + tensor starts).
+inline uint64_t per_call_bytes(uint64_t total_tiles, uint32_t T) {
+  return kCountersBytes + 8 * total_tiles + 8 * (uint64_t)T;
+}
+
+// ------------------------------------------------------------------ device helpers
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void latch_error(Control* ctl, uint32_t code, uint64_t info) {
+  if (atomicCAS(&ctl->error, 0u, code) == 0u) {
+    *reinterpret_cast<volatile uint64_t*>(&ctl->error_info) = info;
+  }
+}
+
+// A bounded wait: returns false once limit_ns has passed since the first call.
+struct WaitClock {
+  uint64_t start = 0;
+  uint32_t backoff = 32;
+  __device__ __forceinline__ bool tick(uint64_t limit_ns) {
+    const uint64_t now = globaltimer_ns();
+    if (start == 0) start = now;
+    if (now - start > limit_ns) return false;
+    __nanosleep(backoff);
+    if (backoff < 512) backoff <<= 1;
+    return true;
+  }
+};
+
+// Decoupled look-back (Merrill and Garland, "Single-pass Parallel Prefix Scan with
+// Decoupled Look-back", 2016), warp-collective: the 32 lanes read the status of the 32
+// nearest predecessors, wait until all of them have published, then add the aggregates
+// up to and including the nearest inclusive prefix. On success *excl is the number of
+// payload words in all tiles before `tile`. Returns false (and latches an error) if a
+// predecessor failed or the wait ran past limit_ns.
+__device__ __forceinline__ bool lookback_exclusive(uint64_t* status, uint64_t tile, uint32_t lane,
+                                                   uint64_t limit_ns, Control* ctl,
+                                                   uint64_t* excl) {
+  uint64_t sum = 0;
+  int64_t top = (int64_t)tile - 1;
+  WaitClock clock;
+  while (true) {
+    const int64_t idx = top - (int64_t)lane;
+    const uint64_t s = (idx >= 0) ? ld_relaxed_u64(status + idx) : (kFlagPrefix << kFlagShift);
+    const uint32_t flag = (uint32_t)(s >> kFlagShift);
+    if (__any_sync(0xffffffffu, flag == kFlagError)) {
+      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
+      return false;
+    }
+    if (__any_sync(0xffffffffu, flag == kFlagInvalid)) {
+      bool alive = true;
+      if (lane == 0) alive = clock.tick(limit_ns);
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+      if (!alive) {
+        if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
+        return false;
+      }
+      continue;
+    }
+    const uint32_t pmask = __ballot_sync(0xffffffffu, flag == kFlagPrefix);
+    uint64_t v = s & kValueMask;
+    if (pmask != 0u && lane > (uint32_t)(__ffs(pmask) - 1)) v = 0;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    sum += v;
+    if (pmask != 0u) break;
+    top -= 32;
+  }
+  *excl = sum;
+  return true;
+}
+
+// Wide decoupled look-back: K rounds of 32 predecessors per pass, so one pass covers
+// 32*K tiles. Load j of lane l reads the tile at distance 32j + l + 1, so each load
+// instruction of the warp reads 32 consecutive status words (two cache lines): with every
+// tile of a round looking back over the same few lines at once, uncoalesced reads would
+// queue up on those L2 lines. The nearest inclusive prefix is the smallest distance with
+// a prefix flag; every entry up to it counts.
+template <int K>
+__device__ __forceinline__ bool lookback_exclusive_wide(uint64_t* status, uint64_t tile,
+                                                        uint32_t lane, uint64_t limit_ns,
+                                                        Control* ctl, uint64_t* excl) {
+  uint64_t sum = 0;
+  int64_t top = (int64_t)tile - 1;
+  WaitClock clock;
+  while (true) {
+    uint64_t s[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      const int64_t idx = top - 32 * j - (int64_t)lane;
+      s[j] = (idx >= 0) ? ld_relaxed_u64(status + idx) : (kFlagPrefix << kFlagShift);
+    }
+    int jstar = K;
+    uint32_t lstar = 31;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      const uint32_t b = __ballot_sync(0xffffffffu, (s[j] >> kFlagShift) == kFlagPrefix);
+      if (b != 0u && jstar == K) {
+        jstar = j;
+        lstar = (uint32_t)(__ffs(b) - 1);
+      }
+    }
+    bool unpublished = false, failed = false;
+    uint64_t part = 0;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      if (j < jstar || (j == jstar && lane <= lstar)) {
+        const uint64_t f = s[j] >> kFlagShift;
+        unpublished |= (f == kFlagInvalid);
+        failed |= (f == kFlagError);
+        part += s[j] & kValueMask;
+      }
+    }
+    if (__any_sync(0xffffffffu, failed)) {
+      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
+      return false;
+    }
+    if (__any_sync(0xffffffffu, unpublished)) {
+      bool alive = true;
+      if (lane == 0) alive = clock.tick(limit_ns);
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+      if (!alive) {
+        if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
+        return false;
+      }
+      continue;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    sum += part;
+    if (jstar < K) break;
+    top -= 32 * K;
+  }
+  *excl = sum;
+  return true;
+}
+
+// ------------------------------------------------------------------ mbarrier + TMA bulk
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  WaitClock clock;
+  while (!mbar_try_wait(bar, parity)) {
+    if (!clock.tick(limit_ns)) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> shared (TMA), completing `bytes` on the mbarrier. dst, src and
+// bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Records e as this thread's last CUDA error and returns ZVC_ERR_CUDA.
+zvc_status cuda_failure(cudaError_t e);
+
+// Kernel tracing (zvc_trace_start / zvc_trace_stop): when enabled, every kernel launch
+// is bracketed by CUDA events recorded on its own stream.
+enum TraceKind { kTraceCompress = 0, kTraceDecompress = 1, kTraceKinds = 2 };
+struct TraceMark {
+  cudaEvent_t stop = nullptr;  // null when tracing is off
+};
+TraceMark trace_begin(int kind, cudaStream_t stream);
+void trace_end(TraceMark m, cudaStream_t stream);
+
+// ------------------------------------------------------------------ launch plans
+struct TensorIn {
+  const uint32_t* ptr;
+  uint64_t n;
+};
+struct TensorOut {
+  uint32_t* ptr;
+  uint64_t n;
+};
+
+// Compress T tensors (T == 1 and !batched: a single stream) into `out`.
+zvc_status launch_compress(const TensorIn* ts, uint32_t T, bool batched, uint32_t chunk_elems,
+                           uint32_t* out, uint64_t out_words, uint64_t* out_size, uint8_t* ws,
+                           uint64_t wait_limit_ns, cudaStream_t stream);
+
+// Decompress a single stream (!batched, T == 1) or a batch of T streams.
+zvc_status launch_decompress(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts,
+                             uint32_t T, bool batched, uint32_t chunk_elems, uint8_t* ws,
+                             cudaStream_t stream);
+
+// Runs the look-back on a tile whose predecessor never publishes, with the given limit;
+// the wait must give up and latch ZVC_ERR_TIMEOUT. Used by the self-test entry point.
+zvc_status launch_lookback_timeout_probe(uint8_t* ws, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace zvc

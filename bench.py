@@ -1,0 +1,539 @@
+#!/usr/bin/env python3
+"""Benchmark of the ZVC hot path on the AlexNet-shaped activation stack.
+
+One step is the whole path on the 5 conv activations of batch 128 (83,210,240 fp32 words,
+333 MB): every layer is offloaded (compressed on the GPU, compressed bytes copied to
+pinned host memory) and then prefetched in reverse layer order (copied back and
+decompressed), as vDNN offloads activations in forward and prefetches them for backward
+propagation (Rhu et al., "Compressing DMA Engine", section V.D). `value` is uncompressed
+GB/s through that round trip with the activations already in HBM.
+
+The same line reports, measured in the same run:
+  roofline      the dominant kernel's algorithmic bytes (4n read + S written for
+                compress, S read + 4n written for decompress) per device second, against
+                the measured HBM copy bandwidth
+  compress / decompress   each kernel alone over the stack (device buffers)
+  e2e           the step with inputs in pinned host memory: H2D of the inputs and D2H of
+                the restored activations inside the timed region
+  cpu_baseline  the single-threaded CPU oracle on a bounded sample of the same workload
+`--impl reference` times that oracle alone (the pages describe hardware; the oracle is
+the only other implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ZVC compress/decompress GB/s (uncompressed) and % of HBM roofline; ratio"
+WORKLOAD = ("alexnet_stack: batch-128 AlexNet conv activations 96x55x55, 256x27x27, "
+            "384x13x13, 384x13x13, 256x13x13 fp32 = ReLU(x + b_c), non-zero 60/45/35/30/20%")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--chunk-elems", type=int, default=4096)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile", choices=["compress", "decompress"],
+                   help="run a few launches of one kernel on AlexNet layer 0 (149 MB) and "
+                        "exit: the small case for ncu captures")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ multi-rank plumbing
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(backend):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(v: float, device=None) -> float:
+    """Maximum of v over ranks (v itself with one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_per_step: float, world: int, steps: int, max_ms: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time, in GB/s."""
+    return bytes_per_rank_per_step * world * steps / (max_ms / 1e3) / 1e9
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid):
+        self.uuid = gpu_uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        if not inside and rows:  # a timed region shorter than the sampling period
+            inside = [min(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for name, val in zip(names[1:], r[3][1:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "samples": len(inside),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_round_trip(batch: int, chunk_elems: int, budget_s: float):
+    """Times the CPU oracle (encode then decode, i.e. compress -> host -> decompress) on
+    the stack generated at a reduced batch. Returns (GB/s, words processed, seconds,
+    description)."""
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    lib = oracle.load()
+    layers = [x.numpy().view(np.uint32).reshape(-1) for x in
+              workloads.alexnet_stack(device="cpu", batch=batch)]
+    done = 0
+    t0 = time.perf_counter()
+    for w in layers:
+        s = oracle.encode(w, chunk_elems, lib=lib)
+        st, back = oracle.decode(s, w.size, chunk_elems, lib=lib)
+        if st != oracle.OK or not np.array_equal(back, w):
+            raise RuntimeError("oracle round trip failed")
+        done += w.size
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return 4 * done / dt / 1e9, done, dt
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    lib = oracle.load()
+    batch = 4  # 1/32 of the batch-128 stack per step: 2.6 M words
+    layers = [x.numpy().view(np.uint32).reshape(-1) for x in
+              workloads.alexnet_stack(device="cpu", batch=batch)]
+    n = sum(w.size for w in layers)
+
+    def step():
+        for w in layers:
+            s = oracle.encode(w, args.chunk_elems, lib=lib)
+            st, _ = oracle.decode(s, w.size, args.chunk_elems, lib=lib)
+            if st != oracle.OK:
+                raise RuntimeError("oracle decode failed")
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = 4 * n * args.steps / dt / 1e9
+    sample = (f"alexnet_stack at batch {batch} (1/32 of batch 128, {n} words) per step; "
+              "oracle encode + decode, single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "chunk_elems": args.chunk_elems,
+                       "sample_batch": batch},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU leg
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from activation_sparsity_compression_gb300 import build as zbuild
+    zbuild.build()
+    import activation_sparsity_compression_gb300 as zvc
+    import workloads
+
+    C = args.chunk_elems
+    xs = workloads.alexnet_stack(device=dev, seed=1 + 100 * rank)
+    ns = [x.numel() for x in xs]
+    N = sum(ns)
+    L = len(xs)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def ok(st, where):
+        if st != zvc.ZVC_OK:
+            raise zvc.ZvcError(st, where)
+
+    hcap = [zvc.zvc_offload_host_bound(n, C) for n in ns]
+    hbuf = [torch.empty(c, dtype=torch.uint8, pin_memory=True) for c in hcap]
+    ws = [zvc.new_workspace(zvc.zvc_offload_workspace_size(n, C), dev) for n in ns]
+    ys = [torch.empty_like(x) for x in xs]
+    hsize = [0] * L
+
+    def step(inputs=xs, outputs=ys):
+        for l in range(L):
+            st, hsize[l] = zvc.zvc_offload(inputs[l].data_ptr(), ns[l], C, hbuf[l].data_ptr(),
+                                           hcap[l], ws[l].data_ptr(), ws[l].numel(), sh)
+            ok(st, "zvc_offload")
+        for l in reversed(range(L)):
+            ok(zvc.zvc_prefetch(hbuf[l].data_ptr(), hsize[l], outputs[l].data_ptr(), ns[l], C,
+                                ws[l].data_ptr(), ws[l].numel(), sh), "zvc_prefetch")
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize(dev)
+    for l in range(L):
+        ok(zvc.zvc_get_error(ws[l].data_ptr(), sh), "device")
+        if not torch.equal(xs[l].view(torch.int32), ys[l].view(torch.int32)):
+            raise RuntimeError(f"round trip of layer {l} is not bit-exact")
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    ok(zvc.zvc_trace_start(), "trace")
+    w0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    w1 = time.time()
+    barrier()
+    st, trace = zvc.zvc_trace_stop()
+    ok(st, "trace")
+    clocks = sampler.stop(w0, w1)
+    ms = e0.elapsed_time(e1)
+    max_ms = reduce_max(ms, dev)
+    value = whole_job_gbs(4 * N, world, args.steps, max_ms)
+
+    # bytes behind the dominant kernel, from the host copies' batch tables
+    prefixes = [16 + 8 * (-(-n // zvc.zvc_offload_segment_elems(n, C)) + 1) for n in ns]
+    seg_stream_bytes = sum(h - p for h, p in zip(hsize, prefixes))
+    algo_bytes = args.steps * (4 * N + seg_stream_bytes)
+    peak, peak_kind = hbm_peak()
+    kern = max(trace, key=lambda k: trace[k][1])
+    launches, kms = trace[kern]
+    achieved = algo_bytes / (kms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": f"{kern}_kernel", "achieved": achieved, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "avg_launch_us": kms / launches * 1e3,
+                "share_of_step": kms / ms}
+
+    extra = measure_components(args, zvc, torch, xs, ns, C, dev, stream, peak)
+    e2e = measure_e2e(args, zvc, torch, xs, ns, C, dev, stream, step, hsize)
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n_words": N, "chunk_elems": C,
+                       "step": "zvc_offload of 5 layers, then zvc_prefetch in reverse order",
+                       "l2": "inputs larger than L2 (333 MB per step), no flush"},
+            "ratio": extra.pop("ratio"),
+            "link_bytes_per_step": sum(hsize),
+            "roofline": roofline,
+            "gpu_launches": trace["compress"][0] + trace["decompress"][0],
+            "clocks": clocks, "e2e": e2e}
+    line.update(extra)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, words, secs = oracle_round_trip(batch=16, chunk_elems=C, budget_s=20.0)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"alexnet_stack at batch 16: {words} words encoded "
+                                          f"and decoded in {secs:.1f} s, single thread"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def _trace(zvc, fn):
+    zvc.zvc_trace_start()
+    fn()
+    st, t = zvc.zvc_trace_stop()
+    if st != zvc.ZVC_OK:
+        raise zvc.ZvcError(st, "trace")
+    return t
+
+
+def measure_components(args, zvc, torch, xs, ns, C, dev, stream, peak):
+    """Each kernel alone over the stack, and the offload / prefetch calls alone."""
+    sh = stream.cuda_stream
+    reps = max(10, min(args.steps, 50))
+    outs = [torch.empty(zvc.zvc_size_bound(n, C), dtype=torch.uint8, device=dev) for n in ns]
+    sizes = torch.zeros(len(ns), dtype=torch.int64, device=dev)
+    wss = [zvc.new_workspace(zvc.zvc_workspace_size(n, C), dev) for n in ns]
+    ys = [torch.empty_like(x) for x in xs]
+
+    def comp():
+        for l in range(len(ns)):
+            zvc.zvc_compress(xs[l].data_ptr(), ns[l], C, outs[l].data_ptr(), outs[l].numel(),
+                             sizes[l:l + 1].data_ptr(), wss[l].data_ptr(), wss[l].numel(), sh)
+
+    comp()
+    torch.cuda.synchronize(dev)
+    S = [int(v) for v in sizes.cpu()]
+
+    def decomp():
+        for l in range(len(ns)):
+            zvc.zvc_decompress(outs[l].data_ptr(), S[l], ys[l].data_ptr(), ns[l], C,
+                               wss[l].data_ptr(), wss[l].numel(), sh)
+
+    decomp()
+    torch.cuda.synchronize(dev)
+    for w in wss:
+        if zvc.zvc_get_error(w.data_ptr(), sh) != zvc.ZVC_OK:
+            raise RuntimeError("component run latched an error")
+    N = sum(ns)
+    tc = _trace(zvc, lambda: [comp() for _ in range(reps)])["compress"][1]
+    td = _trace(zvc, lambda: [decomp() for _ in range(reps)])["decompress"][1]
+    moved = 4 * N + sum(S)
+    res = {"ratio": 4 * N / sum(S),
+           "compress": {"gbs": reps * 4 * N / (tc / 1e3) / 1e9,
+                        "hbm_gbs": reps * moved / (tc / 1e3) / 1e9,
+                        "hbm_frac": reps * moved / (tc / 1e3) / 1e9 / peak},
+           "decompress": {"gbs": reps * 4 * N / (td / 1e3) / 1e9,
+                          "hbm_gbs": reps * moved / (td / 1e3) / 1e9,
+                          "hbm_frac": reps * moved / (td / 1e3) / 1e9 / peak}}
+
+    # offload alone and prefetch alone (wall time on the stream, events)
+    hcap = [zvc.zvc_offload_host_bound(n, C) for n in ns]
+    hb = [torch.empty(c, dtype=torch.uint8, pin_memory=True) for c in hcap]
+    ows = [zvc.new_workspace(zvc.zvc_offload_workspace_size(n, C), dev) for n in ns]
+    hs = [0] * len(ns)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for _ in range(reps):
+        for l in range(len(ns)):
+            _, hs[l] = zvc.zvc_offload(xs[l].data_ptr(), ns[l], C, hb[l].data_ptr(), hcap[l],
+                                       ows[l].data_ptr(), ows[l].numel(), sh)
+    ev[1].record(stream)
+    for _ in range(reps):
+        for l in range(len(ns)):
+            zvc.zvc_prefetch(hb[l].data_ptr(), hs[l], ys[l].data_ptr(), ns[l], C,
+                             ows[l].data_ptr(), ows[l].numel(), sh)
+    ev[2].record(stream)
+    torch.cuda.synchronize(dev)
+    res["offload_gbs"] = reps * 4 * N / (ev[0].elapsed_time(ev[1]) / 1e3) / 1e9
+    res["prefetch_gbs"] = reps * 4 * N / (ev[1].elapsed_time(ev[2]) / 1e3) / 1e9
+
+    # plain uncompressed pinned copies of the same bytes, for comparison
+    hx = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in ns]
+    ev[0].record(stream)
+    for _ in range(reps):
+        for l in range(len(ns)):
+            hx[l].copy_(xs[l].view(-1), non_blocking=True)
+    ev[1].record(stream)
+    for _ in range(reps):
+        for l in range(len(ns)):
+            ys[l].view(-1).copy_(hx[l], non_blocking=True)
+    ev[2].record(stream)
+    torch.cuda.synchronize(dev)
+    res["plain_d2h_gbs"] = reps * 4 * N / (ev[0].elapsed_time(ev[1]) / 1e3) / 1e9
+    res["plain_h2d_gbs"] = reps * 4 * N / (ev[1].elapsed_time(ev[2]) / 1e3) / 1e9
+    return res
+
+
+def measure_e2e(args, zvc, torch, xs, ns, C, dev, stream, step, hsize):
+    """The step through the same C-ABI calls with the activations in pinned host memory:
+    H2D of the inputs, offload, prefetch, D2H of the restored activations."""
+    hx = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in ns]
+    hy = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in ns]
+    for h, x in zip(hx, xs):
+        h.copy_(x.view(-1))
+    dx = [torch.empty_like(x).view(-1) for x in xs]
+    dy = [torch.empty_like(x).view(-1) for x in xs]
+
+    def e2e_step():
+        for d, h in zip(dx, hx):
+            d.copy_(h, non_blocking=True)
+        step(dx, dy)
+        for h, d in zip(hy, dy):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    for h, x in zip(hy, hx):
+        if not torch.equal(h.view(torch.int32), x.view(torch.int32)):
+            raise RuntimeError("e2e round trip is not bit-exact")
+    reps = max(5, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(reps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    max_ms = reduce_max(e0.elapsed_time(e1), dev)
+    _, world, _ = dist_env()
+    N = sum(ns)
+    return {"value": whole_job_gbs(4 * N, world, reps, max_ms), "unit": "GB/s",
+            "h2d_bytes_per_step": 4 * N + sum(hsize), "d2h_bytes_per_step": sum(hsize) + 4 * N,
+            "steps": reps}
+
+
+def run_profile_case(args):
+    """Two warm-up launches then three measured launches of one kernel on AlexNet layer 0
+    (batch 128 x 96 x 55 x 55 fp32, 60% non-zero); prints their CUDA-event times."""
+    import torch
+
+    from activation_sparsity_compression_gb300 import build as zbuild
+    zbuild.build()
+    import activation_sparsity_compression_gb300 as zvc
+    import workloads
+
+    C = args.chunk_elems
+    g = torch.Generator(device="cuda").manual_seed(1)
+    c, h, w, d = workloads.ALEXNET_LAYERS[0]
+    b = torch.tensor(workloads.alexnet_biases(c, d, 1), device="cuda").view(1, c, 1, 1)
+    x = torch.relu_(torch.randn((128, c, h, w), generator=g, device="cuda").add_(b))
+    n = x.numel()
+    out = torch.empty(zvc.zvc_size_bound(n, C), dtype=torch.uint8, device="cuda")
+    size = torch.zeros(1, dtype=torch.int64, device="cuda")
+    ws = zvc.new_workspace(zvc.zvc_workspace_size(n, C))
+    y = torch.empty_like(x)
+    sh = torch.cuda.current_stream().cuda_stream
+    assert zvc.zvc_compress(x.data_ptr(), n, C, out.data_ptr(), out.numel(), size.data_ptr(),
+                            ws.data_ptr(), ws.numel(), sh) == zvc.ZVC_OK
+    S = int(size.item())
+    if args.profile == "compress":
+        def launch():
+            zvc.zvc_compress(x.data_ptr(), n, C, out.data_ptr(), out.numel(), size.data_ptr(),
+                             ws.data_ptr(), ws.numel(), sh)
+    else:
+        def launch():
+            zvc.zvc_decompress(out.data_ptr(), S, y.data_ptr(), n, C, ws.data_ptr(), ws.numel(), sh)
+    launch()
+    times = []
+    for _ in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        launch()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert zvc.zvc_get_error(ws.data_ptr(), sh) == zvc.ZVC_OK
+    if args.profile == "decompress":
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    moved = 4 * n + S
+    print(json.dumps({"profile": args.profile, "n": n, "stream_bytes": S,
+                      "ms": times[1:], "hbm_gbs": [moved / (t / 1e3) / 1e9 for t in times[1:]]}))
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.profile:
+        return run_profile_case(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,182 @@
+/*
+ * zvc.h: C ABI of the GB300 (sm_103a) zero-value-compression (ZVC) library.
+ *
+ * What it computes. Rhu et al., "Compressing DMA Engine: Leveraging Activation Sparsity
+ * for Training Deep Neural Networks" (arXiv:1705.01626), section V.A "Compression
+ * Algorithm": every 32 consecutive 32-bit activation words are replaced by a 32-bit
+ * zero/non-zero mask followed by the non-zero words, so an all-zero window costs one
+ * 4-byte mask (32x). Section V.B: compressed offsets come from prefix sums of the masks'
+ * population counts. Section V.D ("Software Interface"): a compressed copy call that
+ * reports the compressed size, and offload/prefetch of activation maps with
+ * cudaMemcpyAsync. Section IX: activations stay uncompressed in GPU memory; only the
+ * copies to and from host memory carry compressed data.
+ *
+ * Stream format (little-endian, no padding; the framing is this library's reading, the
+ * paper only fixes the mask-then-words core):
+ *
+ *   +0   u32 magic 0x3143565A ("ZVC1")     +4  u16 version 1     +6  u16 word_bytes 4
+ *   +8   u32 window 32                     +12 u32 chunk_elems C (positive multiple of 32)
+ *   +16  u64 n (words)                     +24 u64 payload_bytes
+ *   +32  u64 chunk_off[ceil(n/C)]: byte offset of each chunk inside the payload
+ *   then the payload: for every window in order, u32 mask (bit i = element i of the
+ *   window, least significant bit first) followed by the words whose bit is set, in
+ *   ascending element order. A word is "zero" iff all 32 bits are clear: -0.0, NaN and
+ *   denormals are kept bit for bit. Mask bits at or beyond n are clear. Chunks are
+ *   independently decodable through chunk_off.
+ *   Compressed size S = 32 + 8*ceil(n/C) + 4*ceil(n/32) + 4*nnz.
+ *
+ * Batch format (zvc_*_batched, zvc_offload): u32 magic 0x4243565A ("ZVCB"), u32 T,
+ *   u64 total_bytes, u64 tensor_off[T+1] (absolute; tensor_off[T] = total_bytes), then T
+ *   complete streams, stream i at tensor_off[i].
+ *
+ * Conventions for every call below.
+ *   - Elements are any 4-byte type, treated as opaque 32-bit words.
+ *   - Pointers named d_* are device pointers, h_* host pointers. All buffers are owned
+ *     by the caller; the library allocates nothing. d_* word buffers must be 4-byte
+ *     aligned; 16-byte alignment takes the vectorised path.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Device work is
+ *     enqueued on it and the call returns without waiting, except where stated.
+ *   - The workspace d_ws is device memory of at least the size the matching
+ *     *_workspace_size() returns, 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE
+ *     (e.g. cudaMemset), and not shared by calls that may run concurrently.
+ *   - Errors found by the host are returned at once. Errors found on the device
+ *     (corrupt input, a look-back wait that timed out) are latched in the workspace and
+ *     reported by zvc_get_error(). The library never traps or aborts a kernel.
+ *   - chunk_elems must be a positive multiple of 32 and at most ZVC_MAX_CHUNK_ELEMS.
+ */
+#ifndef ZVC_H_
+#define ZVC_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int zvc_status;
+
+#define ZVC_OK 0
+#define ZVC_ERR_INVALID_ARG 1      /* bad pointer, size, alignment or parameter */
+#define ZVC_ERR_BUFFER_TOO_SMALL 2 /* output or workspace smaller than required */
+#define ZVC_ERR_CORRUPT 3          /* compressed input is not a valid stream for (n, C) */
+#define ZVC_ERR_TIMEOUT 4          /* a device-side wait gave up (reported via zvc_get_error) */
+#define ZVC_ERR_CUDA 5             /* a CUDA runtime call failed; see zvc_last_cuda_error() */
+
+#define ZVC_WINDOW 32u
+#define ZVC_DEFAULT_CHUNK_ELEMS 4096u
+#define ZVC_MAX_CHUNK_ELEMS 32768u
+#define ZVC_MAX_BATCH 512u          /* tensors per batched call */
+#define ZVC_WORKSPACE_ALIGN 256u
+
+/* Worst-case (all words non-zero) size in bytes of one stream of n words:
+ * 32 + 8*ceil(n/C) + 4*ceil(n/32) + 4*n. Returns 0 if chunk_elems is invalid. */
+uint64_t zvc_size_bound(uint64_t n, uint32_t chunk_elems);
+
+/* Worst-case size of a batch of T streams: 16 + 8*(T+1) + sum of zvc_size_bound.
+ * ns is a host array of T word counts. Returns 0 on invalid arguments. */
+uint64_t zvc_batch_size_bound(const uint64_t* ns, uint32_t T, uint32_t chunk_elems);
+
+/* Workspace bytes for zvc_compress / zvc_decompress of n words (look-back tile status,
+ * counters and the latched error word). */
+uint64_t zvc_workspace_size(uint64_t n, uint32_t chunk_elems);
+
+/* Workspace bytes for the batched calls over the T tensors in ns (host array). */
+uint64_t zvc_batch_workspace_size(const uint64_t* ns, uint32_t T, uint32_t chunk_elems);
+
+/* Compress n words at d_in into one stream at d_out (section V.A; the size report of the
+ * section V.D compressed-copy call). out_cap must be at least zvc_size_bound(n, C). The
+ * stream's byte count is written to the device u64 *d_out_size (if not NULL) when the
+ * work completes. Output is byte-identical to the format above. */
+zvc_status zvc_compress(const void* d_in, uint64_t n, uint32_t chunk_elems, void* d_out,
+                        uint64_t out_cap, uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
+                        void* stream);
+
+/* Decompress the stream of in_bytes bytes at d_in into n words at d_out (inverse of
+ * section V.A: a set mask bit takes the next packed word, a clear bit writes zero).
+ * A stream that is not a valid encoding of n words with chunk_elems C latches
+ * ZVC_ERR_CORRUPT; d_out's contents are then unspecified, and no access leaves
+ * [d_in, d_in + in_bytes) or [d_out, d_out + 4n). */
+zvc_status zvc_decompress(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,
+                          uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream);
+
+/* Compress T tensors in one launch into one batch at d_out. d_ins (device pointers) and
+ * ns are HOST arrays of T entries; T <= ZVC_MAX_BATCH. out_cap >= zvc_batch_size_bound.
+ * The batch's total byte count goes to *d_out_size (device, may be NULL). */
+zvc_status zvc_compress_batched(const void* const* d_ins, const uint64_t* ns, uint32_t T,
+                                uint32_t chunk_elems, void* d_out, uint64_t out_cap,
+                                uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
+                                void* stream);
+
+/* Decompress a batch of in_bytes bytes into T tensors. d_outs (device pointers) and ns are
+ * HOST arrays of T entries. Corruption is latched as for zvc_decompress. */
+zvc_status zvc_decompress_batched(const void* d_in, uint64_t in_bytes, void* const* d_outs,
+                                  const uint64_t* ns, uint32_t T, uint32_t chunk_elems,
+                                  void* d_ws, uint64_t ws_bytes, void* stream);
+
+/* Segment length (words) that zvc_offload uses for a tensor of n words: a whole number
+ * of chunks, about 16 Mi words (64 MiB of fp32). */
+uint64_t zvc_offload_segment_elems(uint64_t n, uint32_t chunk_elems);
+
+/* Host bytes zvc_offload may need: the batch bound over its segments. */
+uint64_t zvc_offload_host_bound(uint64_t n, uint32_t chunk_elems);
+
+/* Workspace bytes for zvc_offload / zvc_prefetch: device staging for the pipelined
+ * segments plus the per-segment kernel workspace. */
+uint64_t zvc_offload_workspace_size(uint64_t n, uint32_t chunk_elems);
+
+/* Offload (section V.D: vDNN offloads activations during forward propagation with
+ * cudaMemcpyAsync, cDMA compresses them on the way). The tensor is cut into segments
+ * of zvc_offload_segment_elems() words; each segment is compressed on `stream` into a
+ * device staging buffer and copied to the pinned host buffer h_pinned with
+ * cudaMemcpyAsync on a side stream, so the copy of segment k overlaps the compression
+ * of segment k+1. h_pinned receives a batch (format above) whose streams are the
+ * segments; it is byte-identical to zvc_compress_batched over the segments.
+ * BLOCKS the calling thread until the last segment's copy has been enqueued (the host
+ * must learn each compressed size before it can enqueue the copy); the copies complete
+ * in `stream` order, and *h_size (host) holds the batch's byte count on return.
+ * h_cap >= zvc_offload_host_bound(n, C). h_pinned must be page-locked. */
+zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void* h_pinned,
+                       uint64_t h_cap, uint64_t* h_size, void* d_ws, uint64_t ws_bytes,
+                       void* stream);
+
+/* Prefetch (section V.D: vDNN prefetches offloaded activations before backward
+ * propagation): copies each segment stream of the batch in h_pinned (h_size bytes, as
+ * written by zvc_offload for n words and chunk_elems C) to device staging with
+ * cudaMemcpyAsync on a side stream and decompresses it into d_out on `stream`, the copy
+ * of segment k+1 overlapping the decompression of segment k. Reads the batch table on
+ * the host (a malformed table returns ZVC_ERR_CORRUPT at once); device-side corruption
+ * is latched as for zvc_decompress. Does not block the calling thread. */
+zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint64_t n,
+                        uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream);
+
+/* Self-test of the device-side wait limit: launches the decoupled look-back of a tile
+ * whose predecessor never publishes, with a wait limit of limit_ns (0 < limit_ns <= 1 s).
+ * The wait gives up and latches ZVC_ERR_TIMEOUT in d_ws (read it with zvc_get_error);
+ * the context stays usable. d_ws needs at least 1024 bytes. */
+zvc_status zvc_selftest_wait_timeout(void* d_ws, uint64_t ws_bytes, uint64_t limit_ns,
+                                     void* stream);
+
+/* Kernel tracing. zvc_trace_start() makes every following kernel launch of this library
+ * (on any stream, from any call, including the launches inside zvc_offload/zvc_prefetch)
+ * record a CUDA event pair on its own stream. zvc_trace_stop() waits for those events,
+ * stops tracing and writes, per kernel kind (index 0 = compress, 1 = decompress), the
+ * number of launches to launches[2] and their summed device time in milliseconds to
+ * device_ms[2] (host arrays). */
+zvc_status zvc_trace_start(void);
+zvc_status zvc_trace_stop(uint64_t* launches, double* device_ms);
+
+/* Synchronises `stream`, returns the first device-side error latched in d_ws since the
+ * last call (ZVC_OK if none) and clears it. */
+zvc_status zvc_get_error(void* d_ws, void* stream);
+
+/* The cudaError_t value behind the most recent ZVC_ERR_CUDA on this thread. */
+int zvc_last_cuda_error(void);
+
+/* A static, human-readable name for a zvc_status. */
+const char* zvc_status_string(zvc_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZVC_H_ */

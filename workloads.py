@@ -10,7 +10,7 @@ decodes anything; it only draws numbers.
 Every generator takes ``device``: on a GPU the draws come from a seeded CUDA generator,
 on the CPU from a seeded CPU generator. The two give different values for the same
 seed; parity tests therefore copy the device tensor to the host before handing it to
-the oracle. ``scale`` shrinks the batch dimension (keeping the per-element
+the oracle. A ``batch`` argument shrinks the batch dimension (keeping the per-element
 distribution) so that CPU runs stay small.
 """
 from __future__ import annotations
@@ -52,16 +52,26 @@ ALEXNET_LAYERS = [  # (C, H, W, non-zero density)
 ]
 
 
+def alexnet_biases(c: int, d: float, seed: int):
+    """Per-channel biases of one layer: b_c = mu + 0.5 * Phi^-1((p(c) + 0.5) / C) with p a
+    seeded permutation of the channels and mu = sqrt(1.25) * Phi^-1(d). The biases are the
+    C mid-quantiles of N(mu, 0.5^2), so the channel average of Phi(b_c), the layer's
+    non-zero fraction, is E[Phi(mu + 0.5 Z)] = Phi(mu / sqrt(1.25)) = d up to the
+    midpoint-rule error, while each channel keeps its own density."""
+    rng = np.random.default_rng(seed)
+    mu = (1.25 ** 0.5) * _PHI_INV(d)
+    q = [(k + 0.5) / c for k in rng.permutation(c)]
+    return [mu + 0.5 * _PHI_INV(v) for v in q]
+
+
 def alexnet_stack(device="cuda", batch: int = 128, seed: int = 1):
-    """Five AlexNet conv activations, ReLU(x + b_c), x ~ N(0,1), per-channel bias
-    b_c ~ N(mu, 0.5^2) with mu = sqrt(1.25) * Phi^-1(d), so that E[Phi(b_c)] = d exactly
-    (x + b_c > 0 with probability Phi(b_c); averaging over b_c gives Phi(mu / sqrt(1.25))).
-    Layer l draws from seed + l."""
+    """Five AlexNet conv activations ReLU(x + b_c), x ~ N(0,1), with the per-channel
+    biases of alexnet_biases (layer l draws from seed + l)."""
     out = []
     for l, (c, h, w, d) in enumerate(ALEXNET_LAYERS):
         g = _gen(device, seed + l)
-        mu = (1.25 ** 0.5) * _PHI_INV(d)
-        b = mu + 0.5 * _randn((1, c, 1, 1), device, g)
+        b = torch.tensor(alexnet_biases(c, d, seed + l), dtype=torch.float32,
+                         device=device).view(1, c, 1, 1)
         x = _randn((batch, c, h, w), device, g)
         out.append(torch.relu_(x.add_(b)))
     return out
