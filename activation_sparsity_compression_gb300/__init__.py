@@ -29,6 +29,7 @@ ZVC_DEFAULT_CHUNK_ELEMS = 4096
 ZVC_MAX_CHUNK_ELEMS = 32768
 ZVC_MAX_BATCH = 512
 ZVC_WORKSPACE_ALIGN = 256
+ZVC_STATIC_MAX_ELEMS = 1 << 29
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libzvc_gb300.so")
@@ -48,6 +49,7 @@ _SIGS = {
     "zvc_batch_workspace_size": (_u64, [ctypes.POINTER(_u64), _u32, _u32]),
     "zvc_compress": (_st, [_vp, _u64, _u32, _vp, _u64, _vp, _vp, _u64, _vp]),
     "zvc_decompress": (_st, [_vp, _u64, _vp, _u64, _u32, _vp, _u64, _vp]),
+    "zvc_compress_static": (_st, [_vp, _u64, _u32, _vp, _u64, _vp, _vp]),
     "zvc_compress_batched": (_st, [ctypes.POINTER(_vp), ctypes.POINTER(_u64), _u32, _u32, _vp,
                                    _u64, _vp, _vp, _u64, _vp]),
     "zvc_decompress_batched": (_st, [_vp, _u64, ctypes.POINTER(_vp), ctypes.POINTER(_u64), _u32,
@@ -129,6 +131,12 @@ def zvc_batch_workspace_size(ns, chunk_elems):
 def zvc_compress(d_in, n, chunk_elems, d_out, out_cap, d_out_size, d_ws, ws_bytes, stream):
     return int(lib().zvc_compress(d_in, n, chunk_elems, d_out, out_cap, d_out_size, d_ws,
                                   ws_bytes, stream))
+
+
+def zvc_compress_static(d_in, n, chunk_elems, d_out, out_cap, d_out_size, stream):
+    """zvc_compress for callers that cannot allocate device memory: no workspace, the
+    scratch is a static device array inside the library (n <= ZVC_STATIC_MAX_ELEMS)."""
+    return int(lib().zvc_compress_static(d_in, n, chunk_elems, d_out, out_cap, d_out_size, stream))
 
 
 def zvc_decompress(d_in, in_bytes, d_out, n, chunk_elems, d_ws, ws_bytes, stream):
