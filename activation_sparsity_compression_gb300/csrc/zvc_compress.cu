@@ -17,8 +17,9 @@
 //   offset  decoupled look-back over the tile status words gives the tile's place in the
 //           payload (each lane reads 10 predecessors per round, so one round covers a
 //           whole round of tiles); chunk starts inside the tile write their chunk_off entry
-//   store   the packed tile is built in shared memory at the destination's alignment and
-//           written with 16-byte streaming stores (scalar stores for the ragged ends)
+//   store   once the tile's place is known, each warp stores its windows straight from
+//           registers: the mask, then the non-zero words at popc(mask & lanes below); the
+//           words of one window are contiguous, so every store instruction is coalesced
 //   header  the CTA owning the last tile writes the stream header(s) (and the batch
 //           table) and the total byte count once that tile knows its place.
 #include "zvc_internal.cuh"
@@ -38,7 +39,7 @@ struct CompressArgs {
   uint32_t chunk_elems;
   uint32_t T;
   uint32_t batched;
-  uint32_t pad;
+  int32_t wpc_log2;  // log2(chunk_elems / 32) when that is a power of two, else -1
   const uint32_t* in[MAXT];
   uint64_t n[MAXT];
   uint64_t tile_begin[MAXT + 1];  // first tile of tensor i; tile_begin[T] = total_tiles
@@ -46,7 +47,6 @@ struct CompressArgs {
   uint64_t payload_base[MAXT];    // hdr_before + this stream's header and table
 };
 
-constexpr uint32_t kStageWords = kTileWindows + kTileElems + 4;
 
 using PerCallCounters = Counters;
 static_assert(sizeof(PerCallCounters) <= kCountersBytes, "counter block");
@@ -56,85 +56,44 @@ __device__ __forceinline__ void put_u64_words(uint32_t* p, uint64_t v) {
   p[1] = (uint32_t)(v >> 32);
 }
 
-// Headers of every stream and the batch table. Runs in the CTA that owns the last tile,
-// once that tile knows its place (so the total payload is known); `failed` is set when
-// that tile gave up, in which case a failure upstream has been latched already.
-template <int MAXT>
-__device__ void finalize(const CompressArgs<MAXT>& a, uint64_t total_payload, bool failed,
-                         const uint64_t* tstart, Control* ctl, uint64_t* pbuf) {
-  const uint32_t tid = threadIdx.x;
-  __shared__ int s_fail;
-  if (tid == 0) {
-    bool bad = failed;
-    // pbuf[i] = payload words before stream i; an empty tensor starts where the next
-    // non-empty one does. A tensor's start is published by its first tile, which runs in
-    // some CTA of this grid; wait (bounded) for it.
-    uint64_t next = total_payload;
-    pbuf[a.T] = total_payload;
-    for (int i = (int)a.T - 1; i >= 0 && !bad; --i) {
-      uint64_t p = next;
-      if (a.tile_begin[i + 1] > a.tile_begin[i]) {
-        p = 0;
-        if (MAXT > 1) {
-          WaitClock clock;
-          while (true) {
-            const uint64_t st = ld_relaxed_u64(tstart + i);
-            if ((st >> kFlagShift) == kFlagPrefix) { p = st & kValueMask; break; }
-            if ((st >> kFlagShift) == kFlagError || !clock.tick(a.wait_limit_ns)) {
-              latch_error(ctl, ZVC_ERR_TIMEOUT, a.total_tiles);
-              bad = true;
-              break;
-            }
-          }
-        }
-      }
-      pbuf[i] = p;
-      next = p;
-    }
-    s_fail = bad;
-    if (bad && a.out_size) *a.out_size = 0;
-  }
-  __syncthreads();
-  if (s_fail) return;
-  for (uint32_t i = tid; i < a.T; i += blockDim.x) {
-    const uint64_t s0 = a.hdr_before[i] + pbuf[i];
-    uint32_t* h = a.out + s0;
-    h[0] = kStreamMagic;
-    h[1] = kVersionWordBytes;
-    h[2] = kWindow;
-    h[3] = a.chunk_elems;
-    put_u64_words(h + 4, a.n[i]);
-    put_u64_words(h + 6, 4 * (pbuf[i + 1] - pbuf[i]));
-    if (a.batched) put_u64_words(a.out + kBatchHeaderWords + 2 * i, 4 * s0);
-  }
-  if (tid == 0) {
-    const uint64_t total_bytes = 4 * (a.hdr_words_end + total_payload);
-    if (a.batched) {
-      a.out[0] = kBatchMagic;
-      a.out[1] = a.T;
-      put_u64_words(a.out + 2, total_bytes);
-      put_u64_words(a.out + kBatchHeaderWords + 2 * a.T, total_bytes);
-    }
-    if (a.out_size) *a.out_size = total_bytes;
-  }
-}
+// Roles of the 14 warps of a CTA. Every role walks the CTA's tiles b, b+G, b+2G, ... in
+// order; tile i of the CTA lives in ring slot i % kSlots together with its metadata, and
+// the roles hand it on through one mbarrier per slot and stage:
+//   full     the producer's TMA copy has landed (or the slot holds a direct tile)
+//   masked   the 4 mask warps have written the tile's masks and offsets and published its
+//            aggregate
+//   settled  a settle warp has found the tile's place in the payload
+//   freed    the 8 store warps have written the tile out; the slot can be refilled
+constexpr int kSlots = 6;
+constexpr int kMaskWarps = 4;                       // warps 0..3
+constexpr int kSettleWarp0 = 4;                     // warps 4, 5: even and odd tiles
+constexpr int kSettleWarps = 2;
+constexpr int kStoreWarp0 = 6;                      // warps 6..13
+constexpr int kStoreWarps = 8;
+constexpr int kRoleThreads = 32 * (kMaskWarps + kSettleWarps + kStoreWarps);  // 448
+constexpr uint32_t kWinPerWarp = kTileWindows / kMaskWarps;      // 32 windows per mask warp
+constexpr uint32_t kWinPerStoreWarp = kTileWindows / kStoreWarps;  // 16 windows per store warp
+constexpr int kLookbackWidth = 10;  // one look-back pass covers 320 tiles: a round of tiles
 
-constexpr int kStages = 4;           // input tiles in flight per CTA
-constexpr int kLookbackWidth = 10;   // look-back pass covers 32 * 10 predecessor tiles
-constexpr int kProducerWarp = kCompressWarps - 1;
+struct SlotMeta {
+  uint32_t mask[kTileWindows];
+  uint32_t woff[kTileWindows];       // window offset inside its warp's 32 windows
+  uint32_t wtot[kMaskWarps];         // payload words of each warp's 32 windows
+  uint32_t agg, valid, ti, ok;
+  uint64_t lt, dst, excl, pstart;
+};
 
 struct __align__(16) CompressShared {
-  uint32_t in[kStages][kTileElems];     // input ring, filled by 1-D TMA bulk copies
-  uint32_t out[2][kStageWords];         // packed tiles k (being written) and k-1 (being stored)
-  uint32_t win_off[2][kTileWindows];    // word offset of each window inside its packed tile
-  uint64_t full[kStages];               // mbarrier per ring slot
-  unsigned long long tile[kStages];
-  uint32_t tensor[kStages];
-  uint32_t direct[kStages];             // 1: slot not filled, consumers read global memory
-  uint32_t warp_words[kCompressWarps];
-  // the tile being stored (k-1), as settled by its look-back
-  uint64_t st_dst, st_excl, st_pstart, st_c0;
-  uint32_t st_words, st_nchunks, st_tensor, st_ok;
+  uint32_t in[kSlots][kTileElems];   // input ring, filled by 1-D TMA bulk copies
+  SlotMeta meta[kSlots];
+  uint64_t full[kSlots], masked[kSlots], settled[kSlots], freed[kSlots];
+  uint64_t handoff[2];               // settle warps: tile i's inclusive prefix is in incl[i % 2]
+  uint64_t incl[2];
+  uint32_t incl_ok[2];
+  unsigned long long tile[kSlots];
+  uint32_t tensor[kSlots];
+  uint32_t direct[kSlots];           // 1: slot not filled by TMA; the mask warps copy it in
+  uint64_t pbuf[ZVC_MAX_BATCH + 1];  // stream starts, for the headers
 };
 
 template <int MAXT>
@@ -152,7 +111,7 @@ __device__ __forceinline__ uint32_t tensor_of_tile(const CompressArgs<MAXT>& a, 
 
 // Producer: starts the copy of tile t into ring slot s. Tiles that are not whole
 // 16-byte-aligned 16 KB blocks (a tensor's ragged last tile, or a tensor whose base is
-// not 16-byte aligned) are marked direct and read by the consumers from global memory.
+// not 16-byte aligned) are marked direct.
 template <int MAXT>
 __device__ __forceinline__ void fill_slot(const CompressArgs<MAXT>& a, CompressShared& sm, int s,
                                           unsigned long long t) {
@@ -177,108 +136,312 @@ __device__ __forceinline__ void fill_slot(const CompressArgs<MAXT>& a, CompressS
   }
 }
 
-// The tile whose packed words wait in sm.out[buf] for their place in the payload.
-struct Pending {
-  uint64_t t;       // tile index
-  uint64_t lt;      // tile index inside its tensor
-  uint32_t ti;      // tensor
-  uint32_t agg;     // packed words
-  uint32_t valid;   // input words
-  bool live;
-};
-
-// Warp 0: settles the place of tile p (its aggregate is already published) and writes
-// what the store step needs into shared memory. s_pre holds a look-back pass issued
-// earlier; it is used if it already resolves the prefix, else the look-back re-reads.
+// Headers of every stream and the batch table (one warp). Runs once the last tile knows
+// its place, which gives the total payload; `failed` is set when that tile gave up, in
+// which case a failure upstream has been latched already.
 template <int MAXT>
-__device__ __forceinline__ void settle(const CompressArgs<MAXT>& a, CompressShared& sm,
-                                       const Pending& p, uint64_t* status, uint64_t* tstart,
-                                       Control* ctl, uint32_t lane) {
-  uint64_t excl = 0;
-  bool ok = true;
-  if (p.t != 0) ok = lookback_exclusive_wide<kLookbackWidth>(status, p.t, lane, a.wait_limit_ns, ctl, &excl);
-  const uint64_t dst = a.payload_base[p.ti] + excl;
-  if (ok && dst + p.agg > a.out_words) {
-    if (lane == 0) latch_error(ctl, ZVC_ERR_BUFFER_TOO_SMALL, p.t);
-    ok = false;
-  }
+__device__ void finalize_warp(const CompressArgs<MAXT>& a, uint64_t total_payload, bool failed,
+                              const uint64_t* tstart, Control* ctl, uint64_t* pbuf,
+                              uint32_t lane) {
+  int bad = failed;
   if (lane == 0) {
-    if (p.t != 0)
-      st_relaxed_u64(status + p.t, ok ? ((kFlagPrefix << kFlagShift) | (excl + p.agg))
-                                      : (kFlagError << kFlagShift));
-    uint64_t pstart = 0;
-    if (MAXT > 1) {
-      if (p.lt == 0) {
-        st_relaxed_u64(tstart + p.ti,
-                       ok ? ((kFlagPrefix << kFlagShift) | excl) : (kFlagError << kFlagShift));
-        pstart = excl;
-      } else if (ok) {
-        // payload words before this tensor, published by its first tile (a lower tile)
-        WaitClock clock;
-        while (true) {
-          const uint64_t st = ld_relaxed_u64(tstart + p.ti);
-          const uint64_t f = st >> kFlagShift;
-          if (f == kFlagPrefix) { pstart = st & kValueMask; break; }
-          if (f == kFlagError || !clock.tick(a.wait_limit_ns)) {
-            latch_error(ctl, ZVC_ERR_TIMEOUT, p.t);
-            ok = false;
-            break;
+    // pbuf[i] = payload words before stream i; an empty tensor starts where the next
+    // non-empty one does. A tensor's start is published by its first tile, which runs in
+    // some CTA of this grid; wait (bounded) for it.
+    uint64_t next = total_payload;
+    pbuf[a.T] = total_payload;
+    for (int i = (int)a.T - 1; i >= 0 && !bad; --i) {
+      uint64_t p = next;
+      if (a.tile_begin[i + 1] > a.tile_begin[i]) {
+        p = 0;
+        if (MAXT > 1) {
+          WaitClock clock;
+          while (true) {
+            const uint64_t st = ld_relaxed_u64(tstart + i);
+            if ((st >> kFlagShift) == kFlagPrefix) { p = st & kValueMask; break; }
+            if ((st >> kFlagShift) == kFlagError || !clock.tick(a.wait_limit_ns)) {
+              latch_error(ctl, ZVC_ERR_TIMEOUT, a.total_tiles);
+              bad = 1;
+              break;
+            }
           }
         }
       }
+      pbuf[i] = p;
+      next = p;
     }
-    // chunks whose first window lies in this tile
-    const uint32_t wpc = a.chunk_elems / kWindow;
-    const uint64_t w0 = p.lt * kTileWindows;
-    const uint64_t c0 = ceil_div_u64(w0, wpc);
-    const uint64_t wend = w0 + (p.valid + kWindow - 1) / kWindow;
-    sm.st_c0 = c0;
-    sm.st_nchunks = c0 * wpc < wend ? (uint32_t)((wend - 1 - c0 * wpc) / wpc + 1) : 0u;
-    sm.st_dst = dst;
-    sm.st_excl = excl;
-    sm.st_pstart = pstart;
-    sm.st_words = p.agg;
-    sm.st_tensor = p.ti;
-    sm.st_ok = ok;
+    if (bad && a.out_size) *a.out_size = 0;
+  }
+  bad = __shfl_sync(0xffffffffu, bad, 0);
+  __syncwarp();
+  if (bad) return;
+  for (uint32_t i = lane; i < a.T; i += 32) {
+    const uint64_t s0 = a.hdr_before[i] + pbuf[i];
+    uint32_t* h = a.out + s0;
+    h[0] = kStreamMagic;
+    h[1] = kVersionWordBytes;
+    h[2] = kWindow;
+    h[3] = a.chunk_elems;
+    put_u64_words(h + 4, a.n[i]);
+    put_u64_words(h + 6, 4 * (pbuf[i + 1] - pbuf[i]));
+    if (a.batched) put_u64_words(a.out + kBatchHeaderWords + 2 * i, 4 * s0);
+  }
+  if (lane == 0) {
+    const uint64_t total_bytes = 4 * (a.hdr_words_end + total_payload);
+    if (a.batched) {
+      a.out[0] = kBatchMagic;
+      a.out[1] = a.T;
+      put_u64_words(a.out + 2, total_bytes);
+      put_u64_words(a.out + kBatchHeaderWords + 2 * a.T, total_bytes);
+    }
+    if (a.out_size) *a.out_size = total_bytes;
   }
 }
 
-// All threads: writes the settled tile from sm.out[buf] to its place, at 16-byte stores
-// where the destination allows, and its chunk table entries.
+// Barrier of the four mask warps only (hardware barrier 1; barrier 0 is the CTA's).
+__device__ __forceinline__ void mask_warps_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kMaskWarps * 32) : "memory");
+}
+
+// The same barrier, returning whether any mask thread passed `c`: keeps every mask warp on
+// the same path, so none can leave while the others wait at the barrier.
+__device__ __forceinline__ bool mask_warps_any(bool c) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)c), "n"(kMaskWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+// ---- mask warps: masks, in-warp offsets and the tile's aggregate
 template <int MAXT>
-__device__ __forceinline__ void store_tile(const CompressArgs<MAXT>& a, CompressShared& sm,
-                                           int buf, uint64_t lt, uint32_t tid) {
-  if (!sm.st_ok) return;
-  const uint64_t dst = sm.st_dst;
-  const uint32_t words = sm.st_words;
-  const uint32_t ti = sm.st_tensor;
-  const uint32_t* src = sm.out[buf];
-  const uint32_t wpc = a.chunk_elems / kWindow;
-  const uint64_t w0 = lt * kTileWindows;
-  for (uint32_t k = tid; k < sm.st_nchunks; k += kCompressThreads) {
-    const uint64_t c = sm.st_c0 + k;
-    put_u64_words(a.out + a.hdr_before[ti] + sm.st_pstart + kStreamHeaderWords + 2 * c,
-                  4 * (sm.st_excl - sm.st_pstart + sm.win_off[buf][(uint32_t)(c * wpc - w0)]));
-  }
-  const uint32_t phase = (uint32_t)((reinterpret_cast<uintptr_t>(a.out + dst) >> 2) & 3u);
-  uint32_t* g = a.out + dst - phase;  // 16-byte aligned; word w of g is packed word w - phase
-  const uint32_t span = phase + words;
-  for (uint32_t u = tid; 4u * u < span; u += kCompressThreads) {
-    const uint32_t w = 4u * u;
-    if (w >= phase && w + 4u <= span) {
-      const uint4 q = make_uint4(src[w - phase], src[w + 1 - phase], src[w + 2 - phase],
-                                 src[w + 3 - phase]);
-      __stcs(reinterpret_cast<uint4*>(g + w), q);
-    } else {
+__device__ void mask_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint64_t* status,
+                          Control* ctl, uint32_t warp, uint32_t lane) {
+  for (uint32_t i = 0;; ++i) {
+    const int s = (int)(i % kSlots);
+    if (mask_warps_any(!mbar_wait(&sm.full[s], (i / kSlots) & 1u, a.wait_limit_ns))) {
+      if (warp == 0 && lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, i);
+      return;
+    }
+    const uint64_t t = sm.tile[s];
+    if (t >= a.total_tiles) return;
+    const uint32_t ti = sm.tensor[s];
+    const uint64_t lt = t - a.tile_begin[ti];
+    const uint32_t valid = (uint32_t)min((uint64_t)kTileElems, a.n[ti] - lt * kTileElems);
+    uint32_t* tile = sm.in[s];
+    const uint32_t w0 = warp * kWinPerWarp;  // first window of this warp
+    if (sm.direct[s]) {  // copy this warp's quarter of a ragged or unaligned tile in
+      const uint32_t* src = a.in[ti] + lt * kTileElems;
+      for (uint32_t k = w0 * kWindow + lane; k < (w0 + kWinPerWarp) * kWindow; k += 32)
+        tile[k] = k < valid ? __ldcs(src + k) : 0u;
+      __syncwarp();
+    }
+    // window j of this warp is words 32(w0 + j) ..; lane l reads word l, so the ballot is
+    // the window's mask; lane j keeps window j's
+    uint32_t my_mask = 0;
+#pragma unroll 8
+    for (uint32_t j = 0; j < kWinPerWarp; ++j) {
+      const uint32_t b = __ballot_sync(0xffffffffu, tile[(w0 + j) * kWindow + lane] != 0u);
+      my_mask = (lane == j) ? b : my_mask;
+    }
+    const uint32_t wsz = (w0 + lane) * kWindow < valid ? 1u + __popc(my_mask) : 0u;
+    uint32_t incl = wsz;
 #pragma unroll
-      for (uint32_t j = 0; j < 4; ++j)
-        if (w + j >= phase && w + j < span) g[w + j] = src[w + j - phase];
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= (uint32_t)d) incl += y;
     }
+    SlotMeta& m = sm.meta[s];
+    m.mask[w0 + lane] = my_mask;
+    m.woff[w0 + lane] = incl - wsz;
+    if (lane == 31) m.wtot[warp] = incl;
+    mask_warps_sync();  // all four warp totals are in
+    if (warp == 0 && lane == 0) {
+      uint32_t agg = 0;
+#pragma unroll
+      for (int w = 0; w < kMaskWarps; ++w) agg += m.wtot[w];
+      m.agg = agg;
+      m.valid = valid;
+      m.ti = ti;
+      m.lt = lt;
+      // publish the aggregate now (tile 0 is its own inclusive prefix)
+      st_relaxed_u64(status + t, t == 0 ? ((kFlagPrefix << kFlagShift) | agg)
+                                        : ((kFlagAggregate << kFlagShift) | agg));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.masked[s]);
+  }
+}
+
+// ---- settle warps: each tile's place in the payload. Tile i of the CTA follows the CTA's
+// tile i-1 = t - G, whose inclusive prefix is known by then, so tile t needs only the
+// aggregates of the G - 1 tiles in between (or a nearer published prefix), which every
+// CTA's mask warps publish well ahead: no settle waits for another CTA's settle. Two
+// warps take alternate tiles; each evaluates its look-back pass on its own and only adds
+// the previous tile's inclusive prefix, handed over through shared memory.
+template <int MAXT>
+__device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint64_t* status,
+                            uint64_t* tstart, Control* ctl, uint32_t k, uint32_t lane) {
+  const unsigned long long G = gridDim.x;
+  uint64_t lb[kLookbackWidth];
+  uint32_t i = k;
+  unsigned long long t = blockIdx.x + k * G;
+  if (t < a.total_tiles)
+    lookback_issue<kLookbackWidth>(status, (int64_t)t - 1, lane, lb, i ? (int64_t)(t - G) : -1, 0);
+  for (; t < a.total_tiles; i += 2, t += 2 * G) {
+    const int s = (int)(i % kSlots);
+    if (!mbar_wait(&sm.masked[s], (i / kSlots) & 1u, a.wait_limit_ns)) {
+      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
+      return;
+    }
+    SlotMeta& m = sm.meta[s];
+    const uint32_t agg = m.agg, ti = m.ti;
+    const uint64_t lt = m.lt;
+    const int64_t floor = i ? (int64_t)(t - G) : -1;
+    uint64_t excl = 0;
+    bool at_floor = true;
+    bool ok = true;
+    if (t != 0)
+      ok = lookback_to_floor<kLookbackWidth>(status, t, lane, a.wait_limit_ns, ctl, lb, floor, &excl,
+                                             &at_floor);
+    if (t + 2 * G < a.total_tiles)  // start this warp's next pass
+      lookback_issue<kLookbackWidth>(status, (int64_t)(t + 2 * G) - 1, lane, lb,
+                                     (int64_t)(t + G), 0);
+    if (i > 0) {  // the CTA's previous tile, from the other settle warp
+      const uint32_t h = (i - 1) & 1u;
+      if (!mbar_wait(&sm.handoff[h], ((i - 1) / 2) & 1u, a.wait_limit_ns)) {
+        if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
+        return;
+      }
+      ok = ok && sm.incl_ok[h];
+      if (at_floor) excl += sm.incl[h];
+    }
+    __syncwarp();  // every lane has read the handoff before it is overwritten two tiles on
+    if (lane == 0) {
+      sm.incl[i & 1u] = excl + agg;
+      sm.incl_ok[i & 1u] = ok;
+      mbar_arrive(&sm.handoff[i & 1u]);
+    }
+    const uint64_t dst = a.payload_base[ti] + excl;
+    if (ok && dst + agg > a.out_words) {
+      if (lane == 0) latch_error(ctl, ZVC_ERR_BUFFER_TOO_SMALL, t);
+      ok = false;
+    }
+    if (lane == 0) {
+      if (t != 0)
+        st_relaxed_u64(status + t, ok ? ((kFlagPrefix << kFlagShift) | (excl + agg))
+                                      : (kFlagError << kFlagShift));
+      uint64_t pstart = 0;
+      if (MAXT > 1) {
+        if (lt == 0) {
+          st_relaxed_u64(tstart + ti, ok ? ((kFlagPrefix << kFlagShift) | excl)
+                                         : (kFlagError << kFlagShift));
+          pstart = excl;
+        } else if (ok) {
+          // payload words before this tensor, published by its first tile (a lower tile)
+          WaitClock clock;
+          while (true) {
+            const uint64_t st = ld_relaxed_u64(tstart + ti);
+            const uint64_t f = st >> kFlagShift;
+            if (f == kFlagPrefix) { pstart = st & kValueMask; break; }
+            if (f == kFlagError || !clock.tick(a.wait_limit_ns)) {
+              latch_error(ctl, ZVC_ERR_TIMEOUT, t);
+              ok = false;
+              break;
+            }
+          }
+        }
+      }
+      m.dst = dst;
+      m.excl = excl;
+      m.pstart = pstart;
+      m.ok = ok;
+      mbar_arrive(&sm.settled[s]);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (t + 1 == a.total_tiles)  // the last tile: its place gives the total payload
+      finalize_warp(a, ok ? excl + agg : 0, !ok, tstart, ctl, sm.pbuf, lane);
+  }
+}
+
+// ---- store warps: each writes its 16 windows of the tile straight to the stream
+template <int MAXT>
+__device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Control* ctl,
+                           uint32_t sw, uint32_t lane) {
+  const unsigned long long G = gridDim.x;
+  const uint32_t lane_below = (1u << lane) - 1u;
+  const uint32_t w0 = sw * kWinPerStoreWarp;  // first window of this warp inside the tile
+  const uint32_t mw = w0 / kWinPerWarp;       // the mask warp that scanned these windows
+  unsigned long long t = blockIdx.x;
+  for (uint32_t i = 0; t < a.total_tiles; ++i, t += G) {
+    const int s = (int)(i % kSlots);
+    const uint32_t par = (i / kSlots) & 1u;
+    if (!mbar_wait(&sm.settled[s], par, a.wait_limit_ns)) {
+      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
+      return;
+    }
+    const SlotMeta& m = sm.meta[s];
+    if (m.ok) {
+      // the tile's input words of these windows, loaded before any store
+      const uint32_t* tile = sm.in[s] + w0 * kWindow;
+      uint32_t v[kWinPerStoreWarp];
+#pragma unroll
+      for (uint32_t j = 0; j < kWinPerStoreWarp; ++j) v[j] = tile[j * kWindow + lane];
+      uint32_t wpre = 0;
+#pragma unroll
+      for (uint32_t w = 0; w < kMaskWarps; ++w) wpre += w < mw ? m.wtot[w] : 0u;
+      const uint32_t valid = m.valid;
+      uint32_t* g = a.out + m.dst + wpre;  // start of the mask warp's payload
+      // lanes 0..15 own one window each: its mask, and the chunk table entry if it starts one
+      if (lane < kWinPerStoreWarp && (w0 + lane) * kWindow < valid) {
+        const uint32_t my_off = m.woff[w0 + lane];
+        g[my_off] = m.mask[w0 + lane];
+        const uint64_t wg = m.lt * kTileWindows + w0 + lane;  // window index in its tensor
+        const uint32_t wpc = a.chunk_elems / kWindow;
+        const bool starts = a.wpc_log2 >= 0 ? (wg & ((1ull << a.wpc_log2) - 1)) == 0 : wg % wpc == 0;
+        if (starts) {
+          const uint64_t c = a.wpc_log2 >= 0 ? (wg >> a.wpc_log2) : wg / wpc;
+          put_u64_words(a.out + a.hdr_before[m.ti] + m.pstart + kStreamHeaderWords + 2 * c,
+                        4 * (m.excl - m.pstart + wpre + my_off));
+        }
+      }
+      const uint4* mq = reinterpret_cast<const uint4*>(&m.mask[w0]);
+      const uint4* oq = reinterpret_cast<const uint4*>(&m.woff[w0]);
+      const uint32_t nwin = valid >= (w0 + kWinPerStoreWarp) * kWindow
+                                ? kWinPerStoreWarp
+                                : (valid > w0 * kWindow ? (valid - w0 * kWindow + kWindow - 1) / kWindow : 0u);
+#pragma unroll
+      for (uint32_t q = 0; q < kWinPerStoreWarp / 4; ++q) {
+        const uint4 m4 = mq[q], o4 = oq[q];
+        const uint32_t mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        const uint32_t oo[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+        for (uint32_t r = 0; r < 4; ++r) {
+          const uint32_t j = 4 * q + r;
+          if (j < nwin && v[j] != 0u) g[oo[r] + 1u + __popc(mm[r] & lane_below)] = v[j];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&sm.freed[s]);
+      if (sw == 0) {  // producer: once all store warps are done, refill the slot
+        if (!mbar_wait(&sm.freed[s], par, a.wait_limit_ns)) {
+          latch_error(ctl, ZVC_ERR_TIMEOUT, t);
+        } else {
+          fill_slot(a, sm, s, t + kSlots * G);
+        }
+      }
+    }
+    __syncwarp();
   }
 }
 
 template <int MAXT>
-__global__ void __launch_bounds__(kCompressThreads, 2)
+__global__ void __launch_bounds__(kRoleThreads, 2)
     compress_kernel(const __grid_constant__ CompressArgs<MAXT> a) {
   extern __shared__ __align__(16) uint8_t dsmem[];
   CompressShared& sm = *reinterpret_cast<CompressShared*>(dsmem);
@@ -288,151 +451,27 @@ __global__ void __launch_bounds__(kCompressThreads, 2)
   const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
 
   if (a.total_tiles == 0) {  // every tensor empty: headers only
-    finalize(a, 0, false, tstart, ctl, reinterpret_cast<uint64_t*>(sm.out));
+    if (warp == 0) finalize_warp(a, 0, false, tstart, ctl, sm.pbuf, lane);
     return;
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.masked[s], kMaskWarps);
+      mbar_init(&sm.settled[s], 1);
+      mbar_init(&sm.freed[s], kStoreWarps);
+    }
+    mbar_init(&sm.handoff[0], 1);
+    mbar_init(&sm.handoff[1], 1);
     fence_mbar_init();
   }
   __syncthreads();
   const unsigned long long G = gridDim.x;
-  if (warp == kProducerWarp && lane == 0)
-    for (int s = 0; s < kStages; ++s) fill_slot(a, sm, s, blockIdx.x + s * G);
-
-  const uint32_t ebase = warp * 512u + lane * 4u;
-  const uint32_t sh = 4u * (lane & 7u);
-  Pending prev;
-  prev.live = false;
-
-  for (uint32_t it = 0;; ++it) {
-    const int slot = (int)(it % kStages);
-    const int buf = (int)(it & 1u);
-    const bool late = !mbar_wait(&sm.full[slot], (it / kStages) & 1u, a.wait_limit_ns);
-    if (__syncthreads_or(late)) {
-      if (tid == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, it);
-      break;
-    }
-    const uint64_t t = sm.tile[slot];
-    const bool have = t < a.total_tiles;
-    if (!have && !prev.live) break;
-
-    Pending cur;
-    cur.live = have;
-    uint32_t wpre = 0;
-    uint32_t v[4][4], mask[4], wsz[4], woff[4];
-    if (have) {
-      cur.t = t;
-      cur.ti = sm.tensor[slot];
-      cur.lt = t - a.tile_begin[cur.ti];
-      const uint64_t e0 = cur.lt * kTileElems;
-      cur.valid = (uint32_t)min((uint64_t)kTileElems, a.n[cur.ti] - e0);
-
-      // ---- load (ring slot, or global memory for a direct tile)
-      if (!sm.direct[slot]) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 q = *reinterpret_cast<const uint4*>(&sm.in[slot][ebase + 128u * k]);
-          v[k][0] = q.x; v[k][1] = q.y; v[k][2] = q.z; v[k][3] = q.w;
-        }
-      } else {
-        const uint32_t* src = a.in[cur.ti] + e0;
-        const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t e = ebase + 128u * k;
-          if (vec && e + 4 <= cur.valid) {
-            const uint4 q = __ldcs(reinterpret_cast<const uint4*>(src + e));
-            v[k][0] = q.x; v[k][1] = q.y; v[k][2] = q.z; v[k][3] = q.w;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[k][j] = (e + j < cur.valid) ? __ldcs(src + e + j) : 0u;
-          }
-        }
-      }
-
-      // ---- masks and window sizes (a window past the end of the tensor has size 0)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t m = ((uint32_t)(v[k][0] != 0u) | ((uint32_t)(v[k][1] != 0u) << 1) |
-                      ((uint32_t)(v[k][2] != 0u) << 2) | ((uint32_t)(v[k][3] != 0u) << 3))
-                     << sh;
-        m |= __shfl_xor_sync(0xffffffffu, m, 1);
-        m |= __shfl_xor_sync(0xffffffffu, m, 2);
-        m |= __shfl_xor_sync(0xffffffffu, m, 4);
-        mask[k] = m;
-        const uint32_t wt = warp * 16u + 4u * k + (lane >> 3);
-        wsz[k] = (wt * kWindow < cur.valid) ? 1u + __popc(m) : 0u;
-      }
-
-      // ---- exclusive scan of window sizes inside the tile
-      uint32_t run = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t x = wsz[k];
-        uint32_t y = __shfl_up_sync(0xffffffffu, x, 8);
-        if (lane >= 8) x += y;
-        y = __shfl_up_sync(0xffffffffu, x, 16);
-        if (lane >= 16) x += y;
-        woff[k] = run + x - wsz[k];
-        run += __shfl_sync(0xffffffffu, x, 31);
-      }
-      if (lane == 0) sm.warp_words[warp] = run;
-    }
-    __syncthreads();  // slot consumed, warp totals visible, tile k-2's store finished
-
-    if (have) {
-      if (warp == kProducerWarp && lane == 0) fill_slot(a, sm, slot, t + kStages * G);
-      uint32_t agg = 0;
-#pragma unroll
-      for (int w = 0; w < kCompressWarps; ++w) {
-        const uint32_t c = sm.warp_words[w];
-        wpre += (w < (int)warp) ? c : 0u;
-        agg += c;
-      }
-      cur.agg = agg;
-      // publish this tile's aggregate now; its place is settled one iteration later
-      if (tid == 0)
-        st_relaxed_u64(status + t, t == 0 ? ((kFlagPrefix << kFlagShift) | agg)
-                                          : ((kFlagAggregate << kFlagShift) | agg));
-
-      // ---- pack tile k at offset 0 of its buffer
-      uint32_t* ob = sm.out[buf];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (wsz[k] == 0u) continue;
-        const uint32_t wo = wpre + woff[k];
-        if ((lane & 7u) == 0u) {
-          ob[wo] = mask[k];
-          sm.win_off[buf][warp * 16u + 4u * k + (lane >> 3)] = wo;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (v[k][j] != 0u) {
-            const uint32_t below = mask[k] & ((1u << (sh + j)) - 1u);
-            ob[wo + 1u + __popc(below)] = v[k][j];
-          }
-        }
-      }
-    }
-
-    // ---- settle and store tile k-1
-    if (prev.live) {
-      if (warp == 0) settle(a, sm, prev, status, tstart, ctl, lane);
-      __syncthreads();
-      store_tile(a, sm, buf ^ 1, prev.lt, tid);
-      if (prev.t + 1 == a.total_tiles) {  // the last tile: its place gives the total
-        const bool ok = sm.st_ok;
-        const uint64_t total = sm.st_excl + sm.st_words;
-        __syncthreads();
-        finalize(a, ok ? total : 0, !ok, tstart, ctl,
-                 reinterpret_cast<uint64_t*>(sm.out[buf ^ 1]));
-      }
-    } else {
-      __syncthreads();
-    }
-    prev = cur;
-  }
+  if (warp == kStoreWarp0 && lane == 0)
+    for (int s = 0; s < kSlots; ++s) fill_slot(a, sm, s, blockIdx.x + s * G);
+  if (warp < kMaskWarps) mask_role(a, sm, status, ctl, warp, lane);
+  else if (warp < kStoreWarp0) settle_role(a, sm, status, tstart, ctl, warp - kSettleWarp0, lane);
+  else store_role(a, sm, ctl, warp - kStoreWarp0, lane);
 }
 
 __global__ void lookback_probe_kernel(uint8_t* ws, uint64_t limit_ns) {
@@ -440,7 +479,7 @@ __global__ void lookback_probe_kernel(uint8_t* ws, uint64_t limit_ns) {
   uint64_t* status = reinterpret_cast<uint64_t*>(ws + kStatusOffset);
   uint64_t excl = 0;
   // tile 1 waits on tile 0, which never publishes
-  lookback_exclusive(status, 1, threadIdx.x & 31u, limit_ns, ctl, &excl);
+  lookback_exclusive_wide<kLookbackWidth>(status, 1, threadIdx.x & 31u, limit_ns, ctl, &excl);
 }
 
 template <int MAXT>
@@ -456,7 +495,8 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
   args.chunk_elems = C;
   args.T = T;
   args.batched = batched ? 1u : 0u;
-  args.pad = 0;
+  const uint32_t wpc = C / kWindow;
+  args.wpc_log2 = (wpc & (wpc - 1)) == 0 ? __builtin_ctz(wpc) : -1;
   uint64_t tiles = 0;
   uint64_t hdr = batched ? (kBatchHeaderWords + 2 * ((uint64_t)T + 1)) : 0;
   for (uint32_t i = 0; i < T; ++i) {
@@ -484,7 +524,7 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_failure(e);
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel<MAXT>,
-                                                           kCompressThreads, smem)) != cudaSuccess)
+                                                           kRoleThreads, smem)) != cudaSuccess)
       return cuda_failure(e);
     resident = sms * (per_sm > 0 ? per_sm : 1);
   }
@@ -493,7 +533,7 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
   const uint64_t grid = tiles == 0 ? 1 : (tiles < (uint64_t)resident ? tiles : (uint64_t)resident);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kCompressThreads);
+  cfg.blockDim = dim3(kRoleThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

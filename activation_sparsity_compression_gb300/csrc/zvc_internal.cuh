@@ -91,41 +91,107 @@ __device__ __forceinline__ void latch_error(Control* ctl, uint32_t code, uint64_
   }
 }
 
-// A bounded wait: returns false once limit_ns has passed since the first call.
+// A bounded wait: returns false once limit_ns has passed since the first call. Between
+// polls of global memory it sleeps briefly (16 ns, doubling up to 64 ns): long enough not
+// to flood the L2 with polls, short enough that a waiter wakes soon after the flag flips.
 struct WaitClock {
   uint64_t start = 0;
-  uint32_t backoff = 32;
+  uint32_t backoff = 16;
   __device__ __forceinline__ bool tick(uint64_t limit_ns) {
     const uint64_t now = globaltimer_ns();
     if (start == 0) start = now;
     if (now - start > limit_ns) return false;
     __nanosleep(backoff);
-    if (backoff < 512) backoff <<= 1;
+    if (backoff < 64) backoff <<= 1;
     return true;
   }
 };
 
 // Decoupled look-back (Merrill and Garland, "Single-pass Parallel Prefix Scan with
-// Decoupled Look-back", 2016), warp-collective: the 32 lanes read the status of the 32
-// nearest predecessors, wait until all of them have published, then add the aggregates
-// up to and including the nearest inclusive prefix. On success *excl is the number of
-// payload words in all tiles before `tile`. Returns false (and latches an error) if a
-// predecessor failed or the wait ran past limit_ns.
-__device__ __forceinline__ bool lookback_exclusive(uint64_t* status, uint64_t tile, uint32_t lane,
-                                                   uint64_t limit_ns, Control* ctl,
-                                                   uint64_t* excl) {
+// Decoupled Look-back", 2016), warp-collective and wide: one pass reads 32*K predecessors. Load j of lane l reads the
+// tile at distance 32j + l + 1, so each load instruction of the warp reads 32 consecutive
+// status words (two cache lines): with every tile of a round looking back over the same
+// few lines at once, uncoalesced reads would queue up on those L2 lines. The nearest
+// inclusive prefix is the smallest distance with a prefix flag; every entry up to it
+// counts. A pass can be issued early (lookback_issue) and evaluated later, so that its
+// L2 round trip overlaps other work.
+template <int K>
+__device__ __forceinline__ void lookback_issue(const uint64_t* status, int64_t top, uint32_t lane,
+                                               uint64_t (&s)[K], int64_t floor = -1,
+                                               uint64_t floor_prefix = 0) {
+  // Entries at or below `floor` are not read: the tile at `floor` acts as an inclusive
+  // prefix of floor_prefix words (the caller's own earlier tile, or "nothing" at -1).
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    const int64_t idx = top - 32 * j - (int64_t)lane;
+    s[j] = idx > floor ? ld_relaxed_u64(status + idx)
+                       : ((kFlagPrefix << kFlagShift) | (idx == floor ? floor_prefix : 0));
+  }
+}
+
+enum LookbackPassResult { kPassPrefix = 0, kPassAllAggregates = 1, kPassUnpublished = 2, kPassFailed = 3 };
+
+// Evaluates one pass (warp-collective). On kPassPrefix / kPassAllAggregates, *part is the
+// sum of the counted entries (the whole window for kPassAllAggregates). Aggregates are at
+// most one tile of words each, so the aggregates of one window sum in 32 bits; only the
+// nearest prefix needs 64.
+template <int K>
+__device__ __forceinline__ int lookback_eval(const uint64_t (&s)[K], uint32_t lane, uint64_t* part,
+                                             uint32_t* prefix_dist = nullptr) {
+  uint32_t jl = K;  // this lane's nearest prefix
+#pragma unroll
+  for (int j = K - 1; j >= 0; --j)
+    if ((s[j] >> kFlagShift) == kFlagPrefix) jl = j;
+  const uint32_t jstar = __reduce_min_sync(0xffffffffu, jl);
+  const uint32_t lanes_at = __ballot_sync(0xffffffffu, jl == jstar);
+  const uint32_t lstar = jstar < K ? (uint32_t)(__ffs(lanes_at) - 1) : 31u;
+  bool unpublished = false, failed = false;
+  uint32_t aggs = 0;
+  uint64_t prefix = 0;
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    const bool counted = (uint32_t)j < jstar || ((uint32_t)j == jstar && lane <= lstar);
+    if (counted) {
+      const uint64_t f = s[j] >> kFlagShift;
+      unpublished |= (f == kFlagInvalid);
+      failed |= (f == kFlagError);
+      if (f == kFlagPrefix) prefix = s[j] & kValueMask;
+      else aggs += (uint32_t)(s[j] & kValueMask);
+    }
+  }
+  if (__any_sync(0xffffffffu, failed)) return kPassFailed;
+  if (__any_sync(0xffffffffu, unpublished)) return kPassUnpublished;
+  aggs = __reduce_add_sync(0xffffffffu, aggs);
+  if (jstar < K) {
+    prefix = __shfl_sync(0xffffffffu, prefix, lstar);
+    *part = prefix + aggs;
+    if (prefix_dist) *prefix_dist = 32 * jstar + lstar + 1;  // distance below the pass's top + 1
+    return kPassPrefix;
+  }
+  *part = aggs;
+  return kPassAllAggregates;
+}
+
+// Completes the look-back of `tile` (warp-collective) starting from a pass `s` already
+// issued for top = tile - 1 (with the same floor). On success *excl is the number of
+// payload words in all tiles before `tile`. Returns false (and latches an error) if a predecessor failed or the wait
+// ran past limit_ns.
+template <int K>
+__device__ __forceinline__ bool lookback_finish(uint64_t* status, uint64_t tile, uint32_t lane,
+                                                uint64_t limit_ns, Control* ctl, uint64_t (&s)[K],
+                                                uint64_t* excl, int64_t floor = -1,
+                                                uint64_t floor_prefix = 0) {
   uint64_t sum = 0;
   int64_t top = (int64_t)tile - 1;
   WaitClock clock;
   while (true) {
-    const int64_t idx = top - (int64_t)lane;
-    const uint64_t s = (idx >= 0) ? ld_relaxed_u64(status + idx) : (kFlagPrefix << kFlagShift);
-    const uint32_t flag = (uint32_t)(s >> kFlagShift);
-    if (__any_sync(0xffffffffu, flag == kFlagError)) {
+    uint64_t part = 0;
+    const int r = lookback_eval<K>(s, lane, &part);
+    if (r == kPassFailed) {
       if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
       return false;
     }
-    if (__any_sync(0xffffffffu, flag == kFlagInvalid)) {
+    if (r == kPassUnpublished) {
       bool alive = true;
       if (lane == 0) alive = clock.tick(limit_ns);
       alive = __shfl_sync(0xffffffffu, alive, 0);
@@ -133,67 +199,37 @@ __device__ __forceinline__ bool lookback_exclusive(uint64_t* status, uint64_t ti
         if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
         return false;
       }
-      continue;
+    } else {
+      sum += part;
+      if (r == kPassPrefix) break;
+      top -= 32 * K;
     }
-    const uint32_t pmask = __ballot_sync(0xffffffffu, flag == kFlagPrefix);
-    uint64_t v = s & kValueMask;
-    if (pmask != 0u && lane > (uint32_t)(__ffs(pmask) - 1)) v = 0;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    sum += v;
-    if (pmask != 0u) break;
-    top -= 32;
+    lookback_issue<K>(status, top, lane, s, floor, floor_prefix);
   }
   *excl = sum;
   return true;
 }
 
-// Wide decoupled look-back: K rounds of 32 predecessors per pass, so one pass covers
-// 32*K tiles. Load j of lane l reads the tile at distance 32j + l + 1, so each load
-// instruction of the warp reads 32 consecutive status words (two cache lines): with every
-// tile of a round looking back over the same few lines at once, uncoalesced reads would
-// queue up on those L2 lines. The nearest inclusive prefix is the smallest distance with
-// a prefix flag; every entry up to it counts.
+// As lookback_finish, for a look-back bounded below by `floor`, the caller's own earlier
+// tile, whose inclusive prefix may not be known yet: the floor is read as a prefix of 0
+// words and *at_floor tells whether the walk ended there, in which case the caller adds
+// the floor tile's inclusive prefix to *excl.
 template <int K>
-__device__ __forceinline__ bool lookback_exclusive_wide(uint64_t* status, uint64_t tile,
-                                                        uint32_t lane, uint64_t limit_ns,
-                                                        Control* ctl, uint64_t* excl) {
+__device__ __forceinline__ bool lookback_to_floor(uint64_t* status, uint64_t tile, uint32_t lane,
+                                                  uint64_t limit_ns, Control* ctl, uint64_t (&s)[K],
+                                                  int64_t floor, uint64_t* excl, bool* at_floor) {
   uint64_t sum = 0;
   int64_t top = (int64_t)tile - 1;
   WaitClock clock;
   while (true) {
-    uint64_t s[K];
-#pragma unroll
-    for (int j = 0; j < K; ++j) {
-      const int64_t idx = top - 32 * j - (int64_t)lane;
-      s[j] = (idx >= 0) ? ld_relaxed_u64(status + idx) : (kFlagPrefix << kFlagShift);
-    }
-    int jstar = K;
-    uint32_t lstar = 31;
-#pragma unroll
-    for (int j = 0; j < K; ++j) {
-      const uint32_t b = __ballot_sync(0xffffffffu, (s[j] >> kFlagShift) == kFlagPrefix);
-      if (b != 0u && jstar == K) {
-        jstar = j;
-        lstar = (uint32_t)(__ffs(b) - 1);
-      }
-    }
-    bool unpublished = false, failed = false;
     uint64_t part = 0;
-#pragma unroll
-    for (int j = 0; j < K; ++j) {
-      if (j < jstar || (j == jstar && lane <= lstar)) {
-        const uint64_t f = s[j] >> kFlagShift;
-        unpublished |= (f == kFlagInvalid);
-        failed |= (f == kFlagError);
-        part += s[j] & kValueMask;
-      }
-    }
-    if (__any_sync(0xffffffffu, failed)) {
+    uint32_t dist = 0;
+    const int r = lookback_eval<K>(s, lane, &part, &dist);
+    if (r == kPassFailed) {
       if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
       return false;
     }
-    if (__any_sync(0xffffffffu, unpublished)) {
+    if (r == kPassUnpublished) {
       bool alive = true;
       if (lane == 0) alive = clock.tick(limit_ns);
       alive = __shfl_sync(0xffffffffu, alive, 0);
@@ -201,16 +237,27 @@ __device__ __forceinline__ bool lookback_exclusive_wide(uint64_t* status, uint64
         if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
         return false;
       }
-      continue;
+    } else {
+      sum += part;
+      if (r == kPassPrefix) {
+        *at_floor = (top + 1 - (int64_t)dist) == floor;
+        break;
+      }
+      top -= 32 * K;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    sum += part;
-    if (jstar < K) break;
-    top -= 32 * K;
+    lookback_issue<K>(status, top, lane, s, floor, 0);
   }
   *excl = sum;
   return true;
+}
+
+template <int K>
+__device__ __forceinline__ bool lookback_exclusive_wide(uint64_t* status, uint64_t tile,
+                                                        uint32_t lane, uint64_t limit_ns,
+                                                        Control* ctl, uint64_t* excl) {
+  uint64_t s[K];
+  lookback_issue<K>(status, (int64_t)tile - 1, lane, s);
+  return lookback_finish<K>(status, tile, lane, limit_ns, ctl, s, excl);
 }
 
 // ------------------------------------------------------------------ mbarrier + TMA bulk
@@ -256,12 +303,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for the phase with the given parity to complete; false after limit_ns.
+// Waits for the phase with the given parity to complete; false after limit_ns. try_wait
+// itself suspends the thread in hardware until the phase completes or a short internal
+// limit passes, so the loop only re-polls and checks the clock: no sleep that would delay
+// the wake-up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  WaitClock clock;
+  const uint64_t start = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (!clock.tick(limit_ns)) return false;
+    if (globaltimer_ns() - start > limit_ns) return false;
   }
   return true;
 }
