@@ -14,9 +14,9 @@
 //           OR-reduced over the 8 lanes by three shuffles (bit i = element i of the window)
 //   scan    window sizes 1 + popc(mask) scanned over the 4 groups by two shuffles, over
 //           the 4 groups of a warp in registers, over the 8 warps through shared memory
-//   offset  decoupled look-back over the tile status words gives the tile's place in the
-//           payload (each lane reads 10 predecessors per round, so one round covers a
-//           whole round of tiles); chunk starts inside the tile write their chunk_off entry
+//   offset  a look-back over the published tile aggregates gives the tile's place in the
+//           payload: the sum of the aggregates back to the CTA's own previous tile, plus
+//           that tile's inclusive prefix; chunk starts inside the tile write their chunk_off
 //   store   once the tile's place is known, each warp stores its windows straight from
 //           registers: the mask, then the non-zero words at popc(mask & lanes below); the
 //           words of one window are contiguous, so every store instruction is coalesced
@@ -57,14 +57,18 @@ __device__ __forceinline__ void put_u64_words(uint32_t* p, uint64_t v) {
 }
 
 // Roles of the 14 warps of a CTA. Every role walks the CTA's tiles b, b+G, b+2G, ... in
-// order; tile i of the CTA lives in ring slot i % kSlots together with its metadata, and
-// the roles hand it on through one mbarrier per slot and stage:
-//   full     the producer's TMA copy has landed (or the slot holds a direct tile)
-//   masked   the 4 mask warps have written the tile's masks and offsets and published its
-//            aggregate
+// order. Tile i of the CTA is copied into input slot i % kInSlots; the mask warps read it
+// there and release the slot at once, keeping only the tile's masks and offsets, in
+// metadata slot i % kMetaSlots. The store warps later read the tile's words again from
+// global memory, where the first read left them in L2. So the mask warps, and the tile
+// aggregates they publish, run up to kMetaSlots tiles ahead of the stores, and a look-back
+// rarely meets an unpublished predecessor. The roles hand a tile on through mbarriers:
+//   full     (input slot) the producer's TMA copy has landed, or the slot holds a direct tile
+//   masked   the 4 mask warps have written masks and offsets and published the aggregate
 //   settled  a settle warp has found the tile's place in the payload
-//   freed    the 8 store warps have written the tile out; the slot can be refilled
-constexpr int kSlots = 6;
+//   stored   the 8 store warps have written the tile out; the metadata slot is free
+constexpr int kInSlots = 4;
+constexpr int kMetaSlots = 16;
 constexpr int kMaskWarps = 4;                       // warps 0..3
 constexpr int kSettleWarp0 = 4;                     // warps 4, 5: even and odd tiles
 constexpr int kSettleWarps = 2;
@@ -77,22 +81,23 @@ constexpr int kLookbackWidth = 10;  // one look-back pass covers 320 tiles: a ro
 
 struct SlotMeta {
   uint32_t mask[kTileWindows];
-  uint32_t woff[kTileWindows];       // window offset inside its warp's 32 windows
-  uint32_t wtot[kMaskWarps];         // payload words of each warp's 32 windows
+  uint32_t woff[kTileWindows];       // window offset inside its mask warp's 32 windows
+  uint32_t wtot[kMaskWarps];         // payload words of each mask warp's 32 windows
   uint32_t agg, valid, ti, ok;
   uint64_t lt, dst, excl, pstart;
 };
 
 struct __align__(16) CompressShared {
-  uint32_t in[kSlots][kTileElems];   // input ring, filled by 1-D TMA bulk copies
-  SlotMeta meta[kSlots];
-  uint64_t full[kSlots], masked[kSlots], settled[kSlots], freed[kSlots];
+  uint32_t in[kInSlots][kTileElems];  // input ring, filled by 1-D TMA bulk copies
+  SlotMeta meta[kMetaSlots];
+  uint64_t full[kInSlots];
+  uint64_t masked[kMetaSlots], settled[kMetaSlots], stored[kMetaSlots];
   uint64_t handoff[2];               // settle warps: tile i's inclusive prefix is in incl[i % 2]
   uint64_t incl[2];
   uint32_t incl_ok[2];
-  unsigned long long tile[kSlots];
-  uint32_t tensor[kSlots];
-  uint32_t direct[kSlots];           // 1: slot not filled by TMA; the mask warps copy it in
+  unsigned long long tile[kInSlots];
+  uint32_t tensor[kInSlots];
+  uint32_t direct[kInSlots];         // 1: slot not filled by TMA; the mask warps copy it in
   uint64_t pbuf[ZVC_MAX_BATCH + 1];  // stream starts, for the headers
 };
 
@@ -218,11 +223,17 @@ __device__ __forceinline__ bool mask_warps_any(bool c) {
 
 // ---- mask warps: masks, in-warp offsets and the tile's aggregate
 template <int MAXT>
-__device__ void mask_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint64_t* status,
+__device__ void mask_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint32_t* aggs,
                           Control* ctl, uint32_t warp, uint32_t lane) {
+  const unsigned long long G = gridDim.x;
   for (uint32_t i = 0;; ++i) {
-    const int s = (int)(i % kSlots);
-    if (mask_warps_any(!mbar_wait(&sm.full[s], (i / kSlots) & 1u, a.wait_limit_ns))) {
+    const int s = (int)(i % kInSlots);
+    const int ms = (int)(i % kMetaSlots);
+    bool late = false;
+    if (i >= kMetaSlots)  // metadata slot free once tile i - kMetaSlots is stored
+      late = !mbar_wait(&sm.stored[ms], ((i - kMetaSlots) / kMetaSlots) & 1u, a.wait_limit_ns);
+    late = late || !mbar_wait(&sm.full[s], (i / kInSlots) & 1u, a.wait_limit_ns);
+    if (mask_warps_any(late)) {
       if (warp == 0 && lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, i);
       return;
     }
@@ -254,12 +265,13 @@ __device__ void mask_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
       const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
       if (lane >= (uint32_t)d) incl += y;
     }
-    SlotMeta& m = sm.meta[s];
+    SlotMeta& m = sm.meta[ms];
     m.mask[w0 + lane] = my_mask;
     m.woff[w0 + lane] = incl - wsz;
     if (lane == 31) m.wtot[warp] = incl;
-    mask_warps_sync();  // all four warp totals are in
+    mask_warps_sync();  // the input slot is read and all four warp totals are in
     if (warp == 0 && lane == 0) {
+      fill_slot(a, sm, s, t + kInSlots * G);  // the slot's next tile
       uint32_t agg = 0;
 #pragma unroll
       for (int w = 0; w < kMaskWarps; ++w) agg += m.wtot[w];
@@ -267,33 +279,31 @@ __device__ void mask_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
       m.valid = valid;
       m.ti = ti;
       m.lt = lt;
-      // publish the aggregate now (tile 0 is its own inclusive prefix)
-      st_relaxed_u64(status + t, t == 0 ? ((kFlagPrefix << kFlagShift) | agg)
-                                        : ((kFlagAggregate << kFlagShift) | agg));
+      st_relaxed_u32(aggs + t, agg);  // publish the aggregate now
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.masked[s]);
+    if (lane == 0) mbar_arrive(&sm.masked[ms]);
   }
 }
 
 // ---- settle warps: each tile's place in the payload. Tile i of the CTA follows the CTA's
 // tile i-1 = t - G, whose inclusive prefix is known by then, so tile t needs only the
-// aggregates of the G - 1 tiles in between (or a nearer published prefix), which every
-// CTA's mask warps publish well ahead: no settle waits for another CTA's settle. Two
-// warps take alternate tiles; each evaluates its look-back pass on its own and only adds
-// the previous tile's inclusive prefix, handed over through shared memory.
+// aggregates of the G - 1 tiles in between, which every CTA's mask warps publish well
+// ahead: no settle waits for another CTA's settle. Two warps take alternate tiles; each
+// sums its window on its own and then adds the previous tile's inclusive prefix, handed
+// over through shared memory.
 template <int MAXT>
-__device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint64_t* status,
+__device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint32_t* aggs,
                             uint64_t* tstart, Control* ctl, uint32_t k, uint32_t lane) {
   const unsigned long long G = gridDim.x;
-  uint64_t lb[kLookbackWidth];
+  uint32_t lb[kLookbackWidth];
   uint32_t i = k;
   unsigned long long t = blockIdx.x + k * G;
   if (t < a.total_tiles)
-    lookback_issue<kLookbackWidth>(status, (int64_t)t - 1, lane, lb, i ? (int64_t)(t - G) : -1, 0);
+    aggsum_issue<kLookbackWidth>(aggs, (int64_t)t - 1, i ? (int64_t)(t - G) : -1, lane, lb);
   for (; t < a.total_tiles; i += 2, t += 2 * G) {
-    const int s = (int)(i % kSlots);
-    if (!mbar_wait(&sm.masked[s], (i / kSlots) & 1u, a.wait_limit_ns)) {
+    const int s = (int)(i % kMetaSlots);
+    if (!mbar_wait(&sm.masked[s], (i / kMetaSlots) & 1u, a.wait_limit_ns)) {
       if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
       return;
     }
@@ -302,14 +312,9 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
     const uint64_t lt = m.lt;
     const int64_t floor = i ? (int64_t)(t - G) : -1;
     uint64_t excl = 0;
-    bool at_floor = true;
-    bool ok = true;
-    if (t != 0)
-      ok = lookback_to_floor<kLookbackWidth>(status, t, lane, a.wait_limit_ns, ctl, lb, floor, &excl,
-                                             &at_floor);
+    bool ok = aggsum_finish<kLookbackWidth>(aggs, t, floor, lane, a.wait_limit_ns, ctl, lb, &excl);
     if (t + 2 * G < a.total_tiles)  // start this warp's next pass
-      lookback_issue<kLookbackWidth>(status, (int64_t)(t + 2 * G) - 1, lane, lb,
-                                     (int64_t)(t + G), 0);
+      aggsum_issue<kLookbackWidth>(aggs, (int64_t)(t + 2 * G) - 1, (int64_t)(t + G), lane, lb);
     if (i > 0) {  // the CTA's previous tile, from the other settle warp
       const uint32_t h = (i - 1) & 1u;
       if (!mbar_wait(&sm.handoff[h], ((i - 1) / 2) & 1u, a.wait_limit_ns)) {
@@ -317,7 +322,7 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
         return;
       }
       ok = ok && sm.incl_ok[h];
-      if (at_floor) excl += sm.incl[h];
+      excl += sm.incl[h];
     }
     __syncwarp();  // every lane has read the handoff before it is overwritten two tiles on
     if (lane == 0) {
@@ -331,9 +336,6 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
       ok = false;
     }
     if (lane == 0) {
-      if (t != 0)
-        st_relaxed_u64(status + t, ok ? ((kFlagPrefix << kFlagShift) | (excl + agg))
-                                      : (kFlagError << kFlagShift));
       uint64_t pstart = 0;
       if (MAXT > 1) {
         if (lt == 0) {
@@ -367,7 +369,9 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
   }
 }
 
-// ---- store warps: each writes its 16 windows of the tile straight to the stream
+// ---- store warps: each writes its 16 windows of the tile straight to the stream. The
+// tile's words are read again from global memory (L2 after the producer's copy), as soon
+// as the tile is masked, so the reads are in flight while the tile is settled.
 template <int MAXT>
 __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Control* ctl,
                            uint32_t sw, uint32_t lane) {
@@ -377,23 +381,29 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
   const uint32_t mw = w0 / kWinPerWarp;       // the mask warp that scanned these windows
   unsigned long long t = blockIdx.x;
   for (uint32_t i = 0; t < a.total_tiles; ++i, t += G) {
-    const int s = (int)(i % kSlots);
-    const uint32_t par = (i / kSlots) & 1u;
-    if (!mbar_wait(&sm.settled[s], par, a.wait_limit_ns)) {
+    const int s = (int)(i % kMetaSlots);
+    const uint32_t par = (i / kMetaSlots) & 1u;
+    if (!mbar_wait(&sm.masked[s], par, a.wait_limit_ns)) {
       if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
       return;
     }
     const SlotMeta& m = sm.meta[s];
-    if (m.ok) {
-      // the tile's input words of these windows, loaded before any store
-      const uint32_t* tile = sm.in[s] + w0 * kWindow;
-      uint32_t v[kWinPerStoreWarp];
+    const uint32_t valid = m.valid;
+    const uint32_t* src = a.in[m.ti] + m.lt * kTileElems + w0 * kWindow;
+    uint32_t v[kWinPerStoreWarp];
 #pragma unroll
-      for (uint32_t j = 0; j < kWinPerStoreWarp; ++j) v[j] = tile[j * kWindow + lane];
+    for (uint32_t j = 0; j < kWinPerStoreWarp; ++j) {
+      const uint32_t e = (w0 + j) * kWindow + lane;
+      v[j] = e < valid ? __ldcs(src + j * kWindow + lane) : 0u;
+    }
+    if (!mbar_wait(&sm.settled[s], par, a.wait_limit_ns)) {
+      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
+      return;
+    }
+    if (m.ok) {
       uint32_t wpre = 0;
 #pragma unroll
       for (uint32_t w = 0; w < kMaskWarps; ++w) wpre += w < mw ? m.wtot[w] : 0u;
-      const uint32_t valid = m.valid;
       uint32_t* g = a.out + m.dst + wpre;  // start of the mask warp's payload
       // lanes 0..15 own one window each: its mask, and the chunk table entry if it starts one
       if (lane < kWinPerStoreWarp && (w0 + lane) * kWindow < valid) {
@@ -410,9 +420,6 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
       }
       const uint4* mq = reinterpret_cast<const uint4*>(&m.mask[w0]);
       const uint4* oq = reinterpret_cast<const uint4*>(&m.woff[w0]);
-      const uint32_t nwin = valid >= (w0 + kWinPerStoreWarp) * kWindow
-                                ? kWinPerStoreWarp
-                                : (valid > w0 * kWindow ? (valid - w0 * kWindow + kWindow - 1) / kWindow : 0u);
 #pragma unroll
       for (uint32_t q = 0; q < kWinPerStoreWarp / 4; ++q) {
         const uint4 m4 = mq[q], o4 = oq[q];
@@ -421,22 +428,12 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
 #pragma unroll
         for (uint32_t r = 0; r < 4; ++r) {
           const uint32_t j = 4 * q + r;
-          if (j < nwin && v[j] != 0u) g[oo[r] + 1u + __popc(mm[r] & lane_below)] = v[j];
+          if (v[j] != 0u) g[oo[r] + 1u + __popc(mm[r] & lane_below)] = v[j];
         }
       }
     }
     __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&sm.freed[s]);
-      if (sw == 0) {  // producer: once all store warps are done, refill the slot
-        if (!mbar_wait(&sm.freed[s], par, a.wait_limit_ns)) {
-          latch_error(ctl, ZVC_ERR_TIMEOUT, t);
-        } else {
-          fill_slot(a, sm, s, t + kSlots * G);
-        }
-      }
-    }
-    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.stored[s]);
   }
 }
 
@@ -446,8 +443,9 @@ __global__ void __launch_bounds__(kRoleThreads, 2)
   extern __shared__ __align__(16) uint8_t dsmem[];
   CompressShared& sm = *reinterpret_cast<CompressShared*>(dsmem);
   Control* ctl = reinterpret_cast<Control*>(a.ws);
-  uint64_t* status = reinterpret_cast<uint64_t*>(a.ws + kStatusOffset);
-  uint64_t* tstart = status + a.total_tiles;
+  // per tile: its aggregate (u32), in the tile-status area of the workspace
+  uint32_t* aggs = reinterpret_cast<uint32_t*>(a.ws + kStatusOffset);
+  uint64_t* tstart = reinterpret_cast<uint64_t*>(a.ws + kStatusOffset) + a.total_tiles;
   const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
 
   if (a.total_tiles == 0) {  // every tensor empty: headers only
@@ -455,11 +453,11 @@ __global__ void __launch_bounds__(kRoleThreads, 2)
     return;
   }
   if (tid == 0) {
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&sm.full[s], 1);
+    for (int s = 0; s < kInSlots; ++s) mbar_init(&sm.full[s], 1);
+    for (int s = 0; s < kMetaSlots; ++s) {
       mbar_init(&sm.masked[s], kMaskWarps);
       mbar_init(&sm.settled[s], 1);
-      mbar_init(&sm.freed[s], kStoreWarps);
+      mbar_init(&sm.stored[s], kStoreWarps);
     }
     mbar_init(&sm.handoff[0], 1);
     mbar_init(&sm.handoff[1], 1);
@@ -467,19 +465,21 @@ __global__ void __launch_bounds__(kRoleThreads, 2)
   }
   __syncthreads();
   const unsigned long long G = gridDim.x;
-  if (warp == kStoreWarp0 && lane == 0)
-    for (int s = 0; s < kSlots; ++s) fill_slot(a, sm, s, blockIdx.x + s * G);
-  if (warp < kMaskWarps) mask_role(a, sm, status, ctl, warp, lane);
-  else if (warp < kStoreWarp0) settle_role(a, sm, status, tstart, ctl, warp - kSettleWarp0, lane);
+  if (warp == 0 && lane == 0)
+    for (int s = 0; s < kInSlots; ++s) fill_slot(a, sm, s, blockIdx.x + s * G);
+  if (warp < kMaskWarps) mask_role(a, sm, aggs, ctl, warp, lane);
+  else if (warp < kStoreWarp0) settle_role(a, sm, aggs, tstart, ctl, warp - kSettleWarp0, lane);
   else store_role(a, sm, ctl, warp - kStoreWarp0, lane);
 }
 
 __global__ void lookback_probe_kernel(uint8_t* ws, uint64_t limit_ns) {
   Control* ctl = reinterpret_cast<Control*>(ws);
-  uint64_t* status = reinterpret_cast<uint64_t*>(ws + kStatusOffset);
-  uint64_t excl = 0;
-  // tile 1 waits on tile 0, which never publishes
-  lookback_exclusive_wide<kLookbackWidth>(status, 1, threadIdx.x & 31u, limit_ns, ctl, &excl);
+  const uint32_t* aggs = reinterpret_cast<const uint32_t*>(ws + kStatusOffset);
+  // tile 1 sums the aggregate of tile 0, which nothing publishes
+  uint32_t v[kLookbackWidth];
+  uint64_t sum = 0;
+  aggsum_issue<kLookbackWidth>(aggs, 0, -1, threadIdx.x & 31u, v);
+  aggsum_finish<kLookbackWidth>(aggs, 1, -1, threadIdx.x & 31u, limit_ns, ctl, v, &sum);
 }
 
 template <int MAXT>

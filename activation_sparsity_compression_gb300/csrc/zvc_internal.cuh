@@ -79,6 +79,16 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -258,6 +268,62 @@ __device__ __forceinline__ bool lookback_exclusive_wide(uint64_t* status, uint64
   uint64_t s[K];
   lookback_issue<K>(status, (int64_t)tile - 1, lane, s);
   return lookback_finish<K>(status, tile, lane, limit_ns, ctl, s, excl);
+}
+
+// Bounded look-back over tile aggregates. Each tile publishes its aggregate (its payload
+// words, at least 1, so 0 means "not yet") in aggs[tile]. A tile whose caller already
+// knows the inclusive prefix of an earlier tile `floor` needs only the sum of the
+// aggregates strictly between floor and itself. One pass reads 32*K of them: load j of
+// lane l reads the tile at distance 32j + l + 1 below `top + 1`, so every warp load
+// instruction reads 32 consecutive words. A window of at most one tile's words per entry
+// sums in 32 bits (32*K * 4224 < 2^32 for K <= 31).
+template <int K>
+__device__ __forceinline__ void aggsum_issue(const uint32_t* aggs, int64_t top, int64_t floor,
+                                             uint32_t lane, uint32_t (&v)[K]) {
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    const int64_t idx = top - 32 * j - (int64_t)lane;
+    v[j] = idx > floor ? ld_relaxed_u32(aggs + idx) : 1u;  // below the floor: a placeholder
+  }
+}
+
+// Sum of aggs(floor, tile) (warp-collective), starting from a pass `v` already issued with
+// top = tile - 1. Returns false (and latches ZVC_ERR_TIMEOUT) if an aggregate is still
+// missing after limit_ns.
+template <int K>
+__device__ __forceinline__ bool aggsum_finish(const uint32_t* aggs, uint64_t tile, int64_t floor,
+                                              uint32_t lane, uint64_t limit_ns, Control* ctl,
+                                              uint32_t (&v)[K], uint64_t* sum_out) {
+  uint64_t sum = 0;
+  int64_t top = (int64_t)tile - 1;
+  WaitClock clock;
+  while (top > floor) {
+    bool missing = false;
+    uint32_t part = 0;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      if (top - 32 * j - (int64_t)lane > floor) {
+        missing |= (v[j] == 0u);
+        part += v[j];
+      }
+    }
+    if (__any_sync(0xffffffffu, missing)) {
+      bool alive = true;
+      if (lane == 0) alive = clock.tick(limit_ns);
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+      if (!alive) {
+        if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
+        return false;
+      }
+    } else {
+      sum += __reduce_add_sync(0xffffffffu, part);
+      top -= 32 * K;
+      if (top <= floor) break;
+    }
+    aggsum_issue<K>(aggs, top, floor, lane, v);
+  }
+  *sum_out = sum;
+  return true;
 }
 
 // ------------------------------------------------------------------ mbarrier + TMA bulk
