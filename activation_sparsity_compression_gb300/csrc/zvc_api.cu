@@ -48,7 +48,6 @@ struct SegPlan {
   uint64_t count;       // segments
   uint64_t kernel_ws;   // workspace bytes for one segment's compress
   uint64_t stage;       // bytes of one staging buffer
-  uint64_t sizes_off;   // offset of the per-buffer size slots
   uint64_t stage_off;   // offset of staging buffer 0
   uint64_t total;       // workspace bytes
 };
@@ -69,8 +68,7 @@ SegPlan seg_plan(uint64_t n, uint32_t c) {
   const uint64_t seg_n = n < p.seg ? n : p.seg;
   p.kernel_ws = compress_ws_bytes(tiles_for(seg_n), 1);
   p.stage = round_up_u64(stream_bound(seg_n, c), ZVC_WORKSPACE_ALIGN);
-  p.sizes_off = p.kernel_ws;
-  p.stage_off = p.sizes_off + ZVC_WORKSPACE_ALIGN;
+  p.stage_off = round_up_u64(p.kernel_ws, ZVC_WORKSPACE_ALIGN);
   p.total = p.stage_off + kPipeDepth * p.stage;
   return p;
 }
@@ -309,12 +307,22 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
                        void* stream) {
   if (!chunk_ok(chunk_elems) || n > kMaxElems || h_pinned == nullptr || h_size == nullptr ||
       d_ws == nullptr || (n > 0 && d_in == nullptr) || !aligned(d_in, 4) ||
-      !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
+      !aligned(h_pinned, 8) || !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
     return ZVC_ERR_INVALID_ARG;
   const SegPlan p = seg_plan(n, chunk_elems);
   if (p.count > UINT32_MAX) return ZVC_ERR_INVALID_ARG;
   if (h_cap < zvc_offload_host_bound(n, chunk_elems) || ws_bytes < p.total)
     return ZVC_ERR_BUFFER_TOO_SMALL;
+  // The kernels store each segment's compressed size straight into the pinned buffer, so
+  // the host learns it without a copy queued behind the previous segment's transfer.
+  // That needs h_pinned mapped into the device's address space, as page-locked memory
+  // is under unified addressing.
+  uint8_t* Hdev = nullptr;
+  if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&Hdev), h_pinned, 0) != cudaSuccess ||
+      Hdev == nullptr) {
+    (void)cudaGetLastError();
+    return ZVC_ERR_INVALID_ARG;
+  }
   Pipe* pipe = nullptr;
   zvc_status st = get_pipe(&pipe);
   if (st != ZVC_OK) return st;
@@ -323,19 +331,20 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
   uint8_t* H = static_cast<uint8_t*>(h_pinned);
-  uint64_t* dsizes = reinterpret_cast<uint64_t*>(ws + p.sizes_off);
   const uint32_t* in = static_cast<const uint32_t*>(d_in);
   const uint64_t S = p.count;
   const uint64_t prefix = batch_prefix((uint32_t)S);
   uint64_t pos = prefix;
   std::vector<uint64_t> offs(S + 1, 0);
 
-  // The compressed size of segment k is copied into its (not yet written) batch-table slot
-  // of the pinned buffer; once the host has seen it, the segment's copy is enqueued.
+  // The compress kernel of segment k writes its compressed size into the segment's (not
+  // yet written) batch-table slot of the pinned buffer; once the host has seen it, the
+  // segment's copy is enqueued. A kernel that fails before its last step leaves the 0 the
+  // host put there.
   auto enqueue_copy = [&](uint64_t k) -> zvc_status {
     const int b = (int)(k % kPipeDepth);
     ZVC_CUDA_TRY(cudaEventSynchronize(pipe->kernel_done[b]));
-    const uint64_t sz = get_u64(H + 16 + 8 * k);
+    const uint64_t sz = *reinterpret_cast<volatile uint64_t*>(H + 16 + 8 * k);
     if (sz == 0 || sz > p.stage || pos + sz > h_cap) return read_latched(d_ws);
     offs[k] = pos;
     ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->kernel_done[b], 0));
@@ -351,11 +360,12 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
     if (k >= (uint64_t)kPipeDepth) ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
     const uint64_t nk = (k + 1 < S) ? p.seg : n - k * p.seg;
     const TensorIn t{in + k * p.seg, nk};
+    *reinterpret_cast<volatile uint64_t*>(H + 16 + 8 * k) = 0;
     st = launch_compress(&t, 1, false, chunk_elems,
                          reinterpret_cast<uint32_t*>(ws + p.stage_off + b * p.stage), p.stage / 4,
-                         dsizes + b, ws, kDefaultWaitLimitNs, s);
+                         reinterpret_cast<uint64_t*>(Hdev + 16 + 8 * k), ws, kDefaultWaitLimitNs,
+                         s);
     if (st != ZVC_OK) return st;
-    ZVC_CUDA_TRY(cudaMemcpyAsync(H + 16 + 8 * k, dsizes + b, 8, cudaMemcpyDeviceToHost, s));
     ZVC_CUDA_TRY(cudaEventRecord(pipe->kernel_done[b], s));
     if (k >= 1 && (st = enqueue_copy(k - 1)) != ZVC_OK) return st;
   }

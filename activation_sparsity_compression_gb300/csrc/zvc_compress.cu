@@ -2,26 +2,27 @@
 // window a 32-bit zero/non-zero mask followed by the non-zero words; section V.B: the
 // compressed offsets are prefix sums of the masks' population counts).
 //
-// A tile is 4096 words. The kernel is persistent and launched cooperatively (every CTA is
-// resident at once): CTA b compresses tiles b, b + G, b + 2G, ... (G = grid size) in that
-// order, so each round of G tiles is compressed side by side and every tile a CTA waits
-// for belongs to a running CTA. A producer lane streams the CTA's next tiles into a ring
-// of shared-memory slots with 1-D TMA bulk copies while the tile in hand is processed.
-// Per tile:
-//   load    each warp reads 512 consecutive words from the slot as 16-byte vectors; lane l
-//           of warp w holds words 512w + 128k + 4l .. +3 for k = 0..3
-//   mask    lanes 8g..8g+7 hold window g of each 128-word group: a 4-bit nibble per lane,
-//           OR-reduced over the 8 lanes by three shuffles (bit i = element i of the window)
-//   scan    window sizes 1 + popc(mask) scanned over the 4 groups by two shuffles, over
-//           the 4 groups of a warp in registers, over the 8 warps through shared memory
-//   offset  a look-back over the published tile aggregates gives the tile's place in the
-//           payload: the sum of the aggregates back to the CTA's own previous tile, plus
-//           that tile's inclusive prefix; chunk starts inside the tile write their chunk_off
-//   store   once the tile's place is known, each warp stores its windows straight from
-//           registers: the mask, then the non-zero words at popc(mask & lanes below); the
-//           words of one window are contiguous, so every store instruction is coalesced
-//   header  the CTA owning the last tile writes the stream header(s) (and the batch
-//           table) and the total byte count once that tile knows its place.
+// A tile is 4096 words (128 windows). The kernel is persistent and launched cooperatively
+// (every CTA is resident at once, one per SM): CTA b compresses tiles b, b + G, b + 2G, ...
+// (G = grid size) in that order, so every tile a CTA waits for belongs to a running CTA.
+// Each CTA keeps a ring of shared-memory slots; a tile's slot goes through four roles:
+//   load    a 1-D TMA bulk copy brings the tile's 16 KB into the slot, 128 words in
+//   pack    a team of 4 warps takes the tile, 32 windows each: every warp reads its
+//           windows' words into registers and takes a ballot per window (the window's mask);
+//           the sizes 1 + popc(mask) give each window's place, the team's 4 totals (through
+//           shared memory) each warp's base, and popc(mask & lanes below) each word's place
+//           inside its window. After a team barrier (every word read) the masks and non-zero
+//           words are written back into the same slot, packed from word 0. The tile's packed
+//           size (its aggregate) is published to the other CTAs before the writes.
+//   settle  the tile's place in the payload: the CTA's previous tile t - G has its inclusive
+//           prefix already, so only the aggregates of the G - 1 tiles in between are summed
+//           (no settle waits for another CTA's settle); two warps take alternate tiles and
+//           hand the inclusive prefix on through shared memory
+//   store   one warp copies the packed tile to its place with coalesced 16-byte stores,
+//           writes the chunk table entries of chunks that start in the tile, and starts the
+//           copy of the slot's next tile
+// The CTA owning the last tile writes the stream header(s), the batch table and the total
+// byte count once that tile knows its place.
 #include "zvc_internal.cuh"
 
 namespace zvc {
@@ -39,14 +40,13 @@ struct CompressArgs {
   uint32_t chunk_elems;
   uint32_t T;
   uint32_t batched;
-  int32_t wpc_log2;  // log2(chunk_elems / 32) when that is a power of two, else -1
+  uint32_t inner_chunks;  // 1 when chunks can start inside a tile (C not a multiple of 4096)
   const uint32_t* in[MAXT];
   uint64_t n[MAXT];
   uint64_t tile_begin[MAXT + 1];  // first tile of tensor i; tile_begin[T] = total_tiles
   uint64_t hdr_before[MAXT];      // header/table words (and batch prefix) before stream i
   uint64_t payload_base[MAXT];    // hdr_before + this stream's header and table
 };
-
 
 using PerCallCounters = Counters;
 static_assert(sizeof(PerCallCounters) <= kCountersBytes, "counter block");
@@ -56,50 +56,55 @@ __device__ __forceinline__ void put_u64_words(uint32_t* p, uint64_t v) {
   p[1] = (uint32_t)(v >> 32);
 }
 
-// Roles of the 14 warps of a CTA. Every role walks the CTA's tiles b, b+G, b+2G, ... in
-// order. Tile i of the CTA is copied into input slot i % kInSlots; the mask warps read it
-// there and release the slot at once, keeping only the tile's masks and offsets, in
-// metadata slot i % kMetaSlots. The store warps later read the tile's words again from
-// global memory, where the first read left them in L2. So the mask warps, and the tile
-// aggregates they publish, run up to kMetaSlots tiles ahead of the stores, and a look-back
-// rarely meets an unpublished predecessor. The roles hand a tile on through mbarriers:
-//   full     (input slot) the producer's TMA copy has landed, or the slot holds a direct tile
-//   masked   the 4 mask warps have written masks and offsets and published the aggregate
+// Warp roles. Tile i of the CTA uses slot i % kSlots and is packed by team i % kTeams,
+// settled by settle warp i % 2 and stored by store warp i % kStoreWarps; kSlots is a
+// multiple of all three, so a slot always meets the same warps. The slot's mbarriers:
+//   full     the TMA copy has landed (or the tile is read from global memory directly)
+//   packed   the 4 warps of the pack team have written the packed tile
 //   settled  a settle warp has found the tile's place in the payload
-//   stored   the 8 store warps have written the tile out; the metadata slot is free
-constexpr int kInSlots = 4;
-constexpr int kMetaSlots = 16;
-constexpr int kMaskWarps = 4;                       // warps 0..3
-constexpr int kSettleWarp0 = 4;                     // warps 4, 5: even and odd tiles
+// The store warp that empties a slot starts its refill, so no barrier marks it empty.
+constexpr int kSlots = 12;
+constexpr uint32_t kInOffset = kTileWindows;                 // input lands 128 words in
+constexpr uint32_t kSlotWords = kInOffset + kTileElems;      // 4224: a dense tile's packed size
+constexpr int kTeamWarps = 4;                                // a pack team: 32 windows per warp
+constexpr int kTeams = 2;                                    // warps 0..3 and 4..7
+constexpr uint32_t kWinPerWarp = kTileWindows / kTeamWarps;  // 32
+constexpr int kSettleWarp0 = kTeams * kTeamWarps;            // warps 8, 9
 constexpr int kSettleWarps = 2;
-constexpr int kStoreWarp0 = 6;                      // warps 6..13
-constexpr int kStoreWarps = 8;
-constexpr int kRoleThreads = 32 * (kMaskWarps + kSettleWarps + kStoreWarps);  // 448
-constexpr uint32_t kWinPerWarp = kTileWindows / kMaskWarps;      // 32 windows per mask warp
-constexpr uint32_t kWinPerStoreWarp = kTileWindows / kStoreWarps;  // 16 windows per store warp
-constexpr int kLookbackWidth = 10;  // one look-back pass covers 320 tiles: a round of tiles
+constexpr int kStoreWarp0 = kSettleWarp0 + kSettleWarps;     // warps 10..12
+constexpr int kStoreWarps = 3;
+constexpr int kRoleThreads = 32 * (kStoreWarp0 + kStoreWarps);  // 416
+constexpr int kLookbackWidth = 5;  // one look-back pass covers 160 tiles: a round of tiles
+static_assert(kSlots % kTeams == 0 && kSlots % kSettleWarps == 0 && kSlots % kStoreWarps == 0,
+              "a slot must always meet the same warps");
+static_assert(kWinPerWarp == 32, "one mask per lane of a pack warp");
 
-struct SlotMeta {
-  uint32_t mask[kTileWindows];
-  uint32_t woff[kTileWindows];       // window offset inside its mask warp's 32 windows
-  uint32_t wtot[kMaskWarps];         // payload words of each mask warp's 32 windows
-  uint32_t agg, valid, ti, ok;
-  uint64_t lt, dst, excl, pstart;
+struct SlotInfo {
+  uint64_t lt;          // tile index inside its tensor
+  uint64_t dst;         // word address of the packed tile in the output
+  uint64_t excl;        // payload words before the tile (all streams)
+  uint64_t pstart;      // payload words before the tile's stream
+  uint32_t ti;          // tensor
+  uint32_t direct;      // 1: not brought in by TMA; the pack warp reads global memory
+  uint32_t valid;       // words of the tile inside its tensor
+  uint32_t agg;         // packed words
+  uint32_t ok;
+  uint32_t pad;
 };
 
 struct __align__(16) CompressShared {
-  uint32_t in[kInSlots][kTileElems];  // input ring, filled by 1-D TMA bulk copies
-  SlotMeta meta[kMetaSlots];
-  uint64_t full[kInSlots];
-  uint64_t masked[kMetaSlots], settled[kMetaSlots], stored[kMetaSlots];
-  uint64_t handoff[2];               // settle warps: tile i's inclusive prefix is in incl[i % 2]
+  uint32_t slot[kSlots][kSlotWords];
+  uint32_t woff[kSlots][kTileWindows];  // window offsets, kept only when chunks start inside tiles
+  SlotInfo info[kSlots];
+  uint32_t team_tot[kTeams][2][kTeamWarps];  // pack warps' payload words, double-buffered
+  uint64_t full[kSlots], packed[kSlots], settled[kSlots];
+  uint64_t handoff[2];  // settle warps: tile i's inclusive prefix is in incl[i % 2]
   uint64_t incl[2];
   uint32_t incl_ok[2];
-  unsigned long long tile[kInSlots];
-  uint32_t tensor[kInSlots];
-  uint32_t direct[kInSlots];         // 1: slot not filled by TMA; the mask warps copy it in
   uint64_t pbuf[ZVC_MAX_BATCH + 1];  // stream starts, for the headers
 };
+
+static_assert(sizeof(CompressShared) <= 227 * 1024, "one CTA per SM must fit");
 
 template <int MAXT>
 __device__ __forceinline__ uint32_t tensor_of_tile(const CompressArgs<MAXT>& a, uint64_t t) {
@@ -114,28 +119,28 @@ __device__ __forceinline__ uint32_t tensor_of_tile(const CompressArgs<MAXT>& a, 
   return lo;
 }
 
-// Producer: starts the copy of tile t into ring slot s. Tiles that are not whole
-// 16-byte-aligned 16 KB blocks (a tensor's ragged last tile, or a tensor whose base is
-// not 16-byte aligned) are marked direct.
+// Starts bringing tile t into slot s (one thread). Tiles that are not whole 16-byte-aligned
+// 16 KB blocks (a tensor's ragged last tile, or a tensor whose base is not 16-byte aligned)
+// are marked direct: the pack warp reads them from global memory.
 template <int MAXT>
 __device__ __forceinline__ void fill_slot(const CompressArgs<MAXT>& a, CompressShared& sm, int s,
                                           unsigned long long t) {
-  sm.tile[s] = t;
-  if (t >= a.total_tiles) {
-    sm.direct[s] = 1;
-    mbar_arrive(&sm.full[s]);
-    return;
-  }
+  if (t >= a.total_tiles) return;
   const uint32_t ti = tensor_of_tile(a, t);
-  sm.tensor[s] = ti;
-  const uint64_t e0 = (t - a.tile_begin[ti]) * kTileElems;
+  const uint64_t lt = t - a.tile_begin[ti];
+  const uint64_t e0 = lt * kTileElems;
   const uint32_t* src = a.in[ti] + e0;
-  const bool whole = a.n[ti] - e0 >= kTileElems && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-  sm.direct[s] = whole ? 0u : 1u;
+  const uint64_t left = a.n[ti] - e0;
+  const bool whole = left >= kTileElems && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  SlotInfo& f = sm.info[s];
+  f.ti = ti;
+  f.lt = lt;
+  f.valid = (uint32_t)(left < kTileElems ? left : kTileElems);
+  f.direct = whole ? 0u : 1u;
   if (whole) {
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(&sm.full[s], kTileElems * 4);
-    bulk_g2s(sm.in[s], src, kTileElems * 4, &sm.full[s]);
+    bulk_g2s(&sm.slot[s][kInOffset], src, kTileElems * 4, &sm.full[s]);
   } else {
     mbar_arrive(&sm.full[s]);
   }
@@ -203,92 +208,115 @@ __device__ void finalize_warp(const CompressArgs<MAXT>& a, uint64_t total_payloa
   }
 }
 
-// Barrier of the four mask warps only (hardware barrier 1; barrier 0 is the CTA's).
-__device__ __forceinline__ void mask_warps_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kMaskWarps * 32) : "memory");
-}
-
-// The same barrier, returning whether any mask thread passed `c`: keeps every mask warp on
-// the same path, so none can leave while the others wait at the barrier.
-__device__ __forceinline__ bool mask_warps_any(bool c) {
+// ---- pack teams
+// Barrier of one pack team (hardware barriers 1 and 2; barrier 0 is the CTA's), returning
+// whether any of its threads passed `c`, so that all four warps take the same path.
+__device__ __forceinline__ bool team_any(uint32_t team, bool c) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, %2, q;\n\t"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, %2, %3, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)c), "n"(kMaskWarps * 32)
+      : "r"((uint32_t)c), "r"(1u + team), "n"(kTeamWarps * 32)
       : "memory");
   return r != 0;
 }
 
-// ---- mask warps: masks, in-warp offsets and the tile's aggregate
+__device__ __forceinline__ void team_sync(uint32_t team) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1u + team), "n"(kTeamWarps * 32) : "memory");
+}
+
+// Writes one window (this lane's word v, the window's mask m) at word pos of the slot and
+// returns the position after it.
+__device__ __forceinline__ uint32_t pack_window(uint32_t* slot, uint32_t pos, uint32_t v,
+                                                uint32_t m, uint32_t lane, uint32_t lane_below) {
+  const uint32_t at = v != 0u ? pos + 1u + __popc(m & lane_below) : pos;
+  slot[at] = v != 0u ? v : m;
+  if (m == 0xffffffffu && lane == 0) slot[pos] = m;
+  return pos + 1u + __popc(m);
+}
+
 template <int MAXT>
-__device__ void mask_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint32_t* aggs,
-                          Control* ctl, uint32_t warp, uint32_t lane) {
+__device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint32_t* aggs,
+                          Control* ctl, uint32_t team, uint32_t q, uint32_t lane) {
   const unsigned long long G = gridDim.x;
-  for (uint32_t i = 0;; ++i) {
-    const int s = (int)(i % kInSlots);
-    const int ms = (int)(i % kMetaSlots);
-    bool late = false;
-    if (i >= kMetaSlots)  // metadata slot free once tile i - kMetaSlots is stored
-      late = !mbar_wait(&sm.stored[ms], ((i - kMetaSlots) / kMetaSlots) & 1u, a.wait_limit_ns);
-    late = late || !mbar_wait(&sm.full[s], (i / kInSlots) & 1u, a.wait_limit_ns);
-    if (mask_warps_any(late)) {
-      if (warp == 0 && lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, i);
+  const uint32_t lane_below = (1u << lane) - 1u;
+  const bool keep_woff = a.inner_chunks != 0;
+  const uint32_t w0 = q * kWinPerWarp;  // this warp's first window
+  uint32_t round = 0;
+  for (uint32_t i = team;; i += kTeams, ++round) {
+    const unsigned long long t = blockIdx.x + (unsigned long long)i * G;
+    if (t >= a.total_tiles) return;
+    const int s = (int)(i % kSlots);
+    const bool late = !mbar_wait(&sm.full[s], (i / kSlots) & 1u, a.wait_limit_ns);
+    if (team_any(team, late)) {
+      if (q == 0 && lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
       return;
     }
-    const uint64_t t = sm.tile[s];
-    if (t >= a.total_tiles) return;
-    const uint32_t ti = sm.tensor[s];
-    const uint64_t lt = t - a.tile_begin[ti];
-    const uint32_t valid = (uint32_t)min((uint64_t)kTileElems, a.n[ti] - lt * kTileElems);
-    uint32_t* tile = sm.in[s];
-    const uint32_t w0 = warp * kWinPerWarp;  // first window of this warp
-    if (sm.direct[s]) {  // copy this warp's quarter of a ragged or unaligned tile in
-      const uint32_t* src = a.in[ti] + lt * kTileElems;
-      for (uint32_t k = w0 * kWindow + lane; k < (w0 + kWinPerWarp) * kWindow; k += 32)
-        tile[k] = k < valid ? __ldcs(src + k) : 0u;
-      __syncwarp();
+    const SlotInfo& f = sm.info[s];
+    uint32_t* slot = sm.slot[s];
+    // read: this lane's word of each of the warp's 32 windows
+    uint32_t v[kWinPerWarp];
+    uint32_t nwin = kTileWindows;
+    if (!f.direct) {
+#pragma unroll
+      for (uint32_t j = 0; j < kWinPerWarp; ++j) v[j] = slot[kInOffset + (w0 + j) * kWindow + lane];
+    } else {  // read from global memory; a ragged tile has fewer windows
+      const uint32_t* src = a.in[f.ti] + f.lt * kTileElems;
+      const uint32_t valid = f.valid;
+      nwin = (valid + kWindow - 1) / kWindow;
+#pragma unroll
+      for (uint32_t j = 0; j < kWinPerWarp; ++j) {
+        const uint32_t e = (w0 + j) * kWindow + lane;
+        v[j] = e < valid ? __ldcs(src + e) : 0u;
+      }
     }
-    // window j of this warp is words 32(w0 + j) ..; lane l reads word l, so the ballot is
-    // the window's mask; lane j keeps window j's
-    uint32_t my_mask = 0;
-#pragma unroll 8
+    // masks and the warp's payload words
+    uint32_t m[kWinPerWarp];
+    uint32_t tot = 0;
+#pragma unroll
     for (uint32_t j = 0; j < kWinPerWarp; ++j) {
-      const uint32_t b = __ballot_sync(0xffffffffu, tile[(w0 + j) * kWindow + lane] != 0u);
-      my_mask = (lane == j) ? b : my_mask;
+      m[j] = __ballot_sync(0xffffffffu, v[j] != 0u);
+      tot += w0 + j < nwin ? 1u + __popc(m[j]) : 0u;
     }
-    const uint32_t wsz = (w0 + lane) * kWindow < valid ? 1u + __popc(my_mask) : 0u;
-    uint32_t incl = wsz;
+    uint32_t* tt = sm.team_tot[team][round & 1u];
+    if (lane == 0) tt[q] = tot;
+    team_sync(team);  // every word of the tile is read and every warp total is in
+    uint32_t pos = 0, agg = 0;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= (uint32_t)d) incl += y;
+    for (uint32_t r = 0; r < kTeamWarps; ++r) {
+      const uint32_t x = tt[r];
+      pos += r < q ? x : 0u;
+      agg += x;
     }
-    SlotMeta& m = sm.meta[ms];
-    m.mask[w0 + lane] = my_mask;
-    m.woff[w0 + lane] = incl - wsz;
-    if (lane == 31) m.wtot[warp] = incl;
-    mask_warps_sync();  // the input slot is read and all four warp totals are in
-    if (warp == 0 && lane == 0) {
-      fill_slot(a, sm, s, t + kInSlots * G);  // the slot's next tile
-      uint32_t agg = 0;
-#pragma unroll
-      for (int w = 0; w < kMaskWarps; ++w) agg += m.wtot[w];
-      m.agg = agg;
-      m.valid = valid;
-      m.ti = ti;
-      m.lt = lt;
+    if (q == 0 && lane == 0) {
       st_relaxed_u32(aggs + t, agg);  // publish the aggregate now
+      sm.info[s].agg = agg;
+    }
+    // write back, packed: one store per window, in which the lanes holding a zero write
+    // the mask (only a window without zeros needs a second store for it)
+    if (nwin == kTileWindows && !keep_woff) {
+#pragma unroll
+      for (uint32_t j = 0; j < kWinPerWarp; ++j) pos = pack_window(slot, pos, v[j], m[j], lane, lane_below);
+    } else {
+#pragma unroll 1
+      for (uint32_t j = 0; j < kWinPerWarp && w0 + j < nwin; ++j) {
+        if (keep_woff && lane == 0) sm.woff[s][w0 + j] = pos;
+        uint32_t vj = 0, mj = 0;
+#pragma unroll
+        for (uint32_t k = 0; k < kWinPerWarp; ++k)
+          if (k == j) { vj = v[k]; mj = m[k]; }
+        pos = pack_window(slot, pos, vj, mj, lane, lane_below);
+      }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.masked[ms]);
+    if (lane == 0) mbar_arrive(&sm.packed[s]);
   }
 }
 
 // ---- settle warps: each tile's place in the payload. Tile i of the CTA follows the CTA's
 // tile i-1 = t - G, whose inclusive prefix is known by then, so tile t needs only the
-// aggregates of the G - 1 tiles in between, which every CTA's mask warps publish well
+// aggregates of the G - 1 tiles in between, which every CTA's pack warps publish well
 // ahead: no settle waits for another CTA's settle. Two warps take alternate tiles; each
 // sums its window on its own and then adds the previous tile's inclusive prefix, handed
 // over through shared memory.
@@ -302,14 +330,14 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
   if (t < a.total_tiles)
     aggsum_issue<kLookbackWidth>(aggs, (int64_t)t - 1, i ? (int64_t)(t - G) : -1, lane, lb);
   for (; t < a.total_tiles; i += 2, t += 2 * G) {
-    const int s = (int)(i % kMetaSlots);
-    if (!mbar_wait(&sm.masked[s], (i / kMetaSlots) & 1u, a.wait_limit_ns)) {
+    const int s = (int)(i % kSlots);
+    if (!mbar_wait(&sm.packed[s], (i / kSlots) & 1u, a.wait_limit_ns)) {
       if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
       return;
     }
-    SlotMeta& m = sm.meta[s];
-    const uint32_t agg = m.agg, ti = m.ti;
-    const uint64_t lt = m.lt;
+    SlotInfo& f = sm.info[s];
+    const uint32_t agg = f.agg, ti = f.ti;
+    const uint64_t lt = f.lt;
     const int64_t floor = i ? (int64_t)(t - G) : -1;
     uint64_t excl = 0;
     bool ok = aggsum_finish<kLookbackWidth>(aggs, t, floor, lane, a.wait_limit_ns, ctl, lb, &excl);
@@ -347,9 +375,9 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
           WaitClock clock;
           while (true) {
             const uint64_t st = ld_relaxed_u64(tstart + ti);
-            const uint64_t f = st >> kFlagShift;
-            if (f == kFlagPrefix) { pstart = st & kValueMask; break; }
-            if (f == kFlagError || !clock.tick(a.wait_limit_ns)) {
+            const uint64_t fl = st >> kFlagShift;
+            if (fl == kFlagPrefix) { pstart = st & kValueMask; break; }
+            if (fl == kFlagError || !clock.tick(a.wait_limit_ns)) {
               latch_error(ctl, ZVC_ERR_TIMEOUT, t);
               ok = false;
               break;
@@ -357,10 +385,10 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
           }
         }
       }
-      m.dst = dst;
-      m.excl = excl;
-      m.pstart = pstart;
-      m.ok = ok;
+      f.dst = dst;
+      f.excl = excl;
+      f.pstart = pstart;
+      f.ok = ok;
       mbar_arrive(&sm.settled[s]);
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -369,76 +397,67 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
   }
 }
 
-// ---- store warps: each writes its 16 windows of the tile straight to the stream. The
-// tile's words are read again from global memory (L2 after the producer's copy), as soon
-// as the tile is masked, so the reads are in flight while the tile is settled.
+// ---- store warps: copy the packed tile out, write its chunk table entries, refill the slot
 template <int MAXT>
 __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Control* ctl,
-                           uint32_t sw, uint32_t lane) {
+                           uint32_t k, uint32_t lane) {
   const unsigned long long G = gridDim.x;
-  const uint32_t lane_below = (1u << lane) - 1u;
-  const uint32_t w0 = sw * kWinPerStoreWarp;  // first window of this warp inside the tile
-  const uint32_t mw = w0 / kWinPerWarp;       // the mask warp that scanned these windows
-  unsigned long long t = blockIdx.x;
-  for (uint32_t i = 0; t < a.total_tiles; ++i, t += G) {
-    const int s = (int)(i % kMetaSlots);
-    const uint32_t par = (i / kMetaSlots) & 1u;
-    if (!mbar_wait(&sm.masked[s], par, a.wait_limit_ns)) {
+  const uint32_t wpc = a.chunk_elems / kWindow;
+  for (uint32_t i = k;; i += kStoreWarps) {
+    const unsigned long long t = blockIdx.x + (unsigned long long)i * G;
+    if (t >= a.total_tiles) return;
+    const int s = (int)(i % kSlots);
+    if (!mbar_wait(&sm.settled[s], (i / kSlots) & 1u, a.wait_limit_ns)) {
       if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
       return;
     }
-    const SlotMeta& m = sm.meta[s];
-    const uint32_t valid = m.valid;
-    const uint32_t* src = a.in[m.ti] + m.lt * kTileElems + w0 * kWindow;
-    uint32_t v[kWinPerStoreWarp];
-#pragma unroll
-    for (uint32_t j = 0; j < kWinPerStoreWarp; ++j) {
-      const uint32_t e = (w0 + j) * kWindow + lane;
-      v[j] = e < valid ? __ldcs(src + j * kWindow + lane) : 0u;
-    }
-    if (!mbar_wait(&sm.settled[s], par, a.wait_limit_ns)) {
-      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
-      return;
-    }
-    if (m.ok) {
-      uint32_t wpre = 0;
-#pragma unroll
-      for (uint32_t w = 0; w < kMaskWarps; ++w) wpre += w < mw ? m.wtot[w] : 0u;
-      uint32_t* g = a.out + m.dst + wpre;  // start of the mask warp's payload
-      // lanes 0..15 own one window each: its mask, and the chunk table entry if it starts one
-      if (lane < kWinPerStoreWarp && (w0 + lane) * kWindow < valid) {
-        const uint32_t my_off = m.woff[w0 + lane];
-        g[my_off] = m.mask[w0 + lane];
-        const uint64_t wg = m.lt * kTileWindows + w0 + lane;  // window index in its tensor
-        const uint32_t wpc = a.chunk_elems / kWindow;
-        const bool starts = a.wpc_log2 >= 0 ? (wg & ((1ull << a.wpc_log2) - 1)) == 0 : wg % wpc == 0;
-        if (starts) {
-          const uint64_t c = a.wpc_log2 >= 0 ? (wg >> a.wpc_log2) : wg / wpc;
-          put_u64_words(a.out + a.hdr_before[m.ti] + m.pstart + kStreamHeaderWords + 2 * c,
-                        4 * (m.excl - m.pstart + wpre + my_off));
+    const SlotInfo& f = sm.info[s];
+    const uint32_t* src = sm.slot[s];
+    if (f.ok) {
+      const uint32_t agg = f.agg;
+      uint32_t* g = a.out + f.dst;
+      // words up to the first 16-byte boundary of the destination, then 16-byte stores
+      const uint32_t head = min(agg, (4u - (uint32_t)((reinterpret_cast<uintptr_t>(g) >> 2) & 3u)) & 3u);
+      if (lane < head) g[lane] = src[lane];
+      const uint32_t nv = (agg - head) >> 2;
+      uint4* gv = reinterpret_cast<uint4*>(g + head);
+      const uint4* sv = reinterpret_cast<const uint4*>(src);
+      if (head == 0) {
+#pragma unroll 4
+        for (uint32_t q = lane; q < nv; q += 32) gv[q] = sv[q];
+      } else {
+#pragma unroll 4
+        for (uint32_t q = lane; q < nv; q += 32) {
+          const uint32_t* p = src + head + 4 * q;
+          gv[q] = make_uint4(p[0], p[1], p[2], p[3]);
         }
       }
-      const uint4* mq = reinterpret_cast<const uint4*>(&m.mask[w0]);
-      const uint4* oq = reinterpret_cast<const uint4*>(&m.woff[w0]);
-#pragma unroll
-      for (uint32_t q = 0; q < kWinPerStoreWarp / 4; ++q) {
-        const uint4 m4 = mq[q], o4 = oq[q];
-        const uint32_t mm[4] = {m4.x, m4.y, m4.z, m4.w};
-        const uint32_t oo[4] = {o4.x, o4.y, o4.z, o4.w};
-#pragma unroll
-        for (uint32_t r = 0; r < 4; ++r) {
-          const uint32_t j = 4 * q + r;
-          if (v[j] != 0u) g[oo[r] + 1u + __popc(mm[r] & lane_below)] = v[j];
+      const uint32_t done = head + 4 * nv;
+      if (lane < agg - done) g[done + lane] = src[done + lane];
+      // chunk table entries of the chunks that start in this tile
+      uint32_t* table = a.out + a.hdr_before[f.ti] + f.pstart + kStreamHeaderWords;
+      const uint64_t in_stream = f.excl - f.pstart;  // payload words of the stream before the tile
+      const uint64_t w_first = f.lt * kTileWindows;
+      if (!a.inner_chunks) {  // chunks are whole tiles: at most window 0 starts one
+        if (lane == 0 && w_first % wpc == 0)
+          put_u64_words(table + 2 * (w_first / wpc), 4 * in_stream);
+      } else {
+        const uint32_t nwin = (f.valid + kWindow - 1) / kWindow;
+        for (uint32_t w = lane; w < nwin; w += 32) {
+          const uint64_t wg = w_first + w;
+          if (wg % wpc == 0) put_u64_words(table + 2 * (wg / wpc), 4 * (in_stream + sm.woff[s][w]));
         }
       }
     }
+    // the slot is read; it takes tile i + kSlots next
+    fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.stored[s]);
+    if (lane == 0) fill_slot(a, sm, s, t + (unsigned long long)kSlots * G);
   }
 }
 
 template <int MAXT>
-__global__ void __launch_bounds__(kRoleThreads, 2)
+__global__ void __launch_bounds__(kRoleThreads, 1)
     compress_kernel(const __grid_constant__ CompressArgs<MAXT> a) {
   extern __shared__ __align__(16) uint8_t dsmem[];
   CompressShared& sm = *reinterpret_cast<CompressShared*>(dsmem);
@@ -453,11 +472,10 @@ __global__ void __launch_bounds__(kRoleThreads, 2)
     return;
   }
   if (tid == 0) {
-    for (int s = 0; s < kInSlots; ++s) mbar_init(&sm.full[s], 1);
-    for (int s = 0; s < kMetaSlots; ++s) {
-      mbar_init(&sm.masked[s], kMaskWarps);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.packed[s], kTeamWarps);
       mbar_init(&sm.settled[s], 1);
-      mbar_init(&sm.stored[s], kStoreWarps);
     }
     mbar_init(&sm.handoff[0], 1);
     mbar_init(&sm.handoff[1], 1);
@@ -465,9 +483,9 @@ __global__ void __launch_bounds__(kRoleThreads, 2)
   }
   __syncthreads();
   const unsigned long long G = gridDim.x;
-  if (warp == 0 && lane == 0)
-    for (int s = 0; s < kInSlots; ++s) fill_slot(a, sm, s, blockIdx.x + s * G);
-  if (warp < kMaskWarps) mask_role(a, sm, aggs, ctl, warp, lane);
+  if (tid == 0)
+    for (int s = 0; s < kSlots; ++s) fill_slot(a, sm, s, blockIdx.x + (unsigned long long)s * G);
+  if (warp < kSettleWarp0) pack_role(a, sm, aggs, ctl, warp / kTeamWarps, warp % kTeamWarps, lane);
   else if (warp < kStoreWarp0) settle_role(a, sm, aggs, tstart, ctl, warp - kSettleWarp0, lane);
   else store_role(a, sm, ctl, warp - kStoreWarp0, lane);
 }
@@ -495,8 +513,7 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
   args.chunk_elems = C;
   args.T = T;
   args.batched = batched ? 1u : 0u;
-  const uint32_t wpc = C / kWindow;
-  args.wpc_log2 = (wpc & (wpc - 1)) == 0 ? __builtin_ctz(wpc) : -1;
+  args.inner_chunks = C % kTileElems != 0 ? 1u : 0u;
   uint64_t tiles = 0;
   uint64_t hdr = batched ? (kBatchHeaderWords + 2 * ((uint64_t)T + 1)) : 0;
   for (uint32_t i = 0; i < T; ++i) {

@@ -14,7 +14,7 @@
 //             the walk must end exactly at the next chunk's offset
 //   scatter   lane l expands words 4(l mod 8) .. +3 of window 4q + l/8: a set bit at
 //             position b reads packed word popc(mask & (2^b - 1)), a clear bit writes 0;
-//             each step writes four whole 128-byte windows with 16-byte stores
+//             each step expands sixteen whole 128-byte windows with 16-byte stores
 // Extra work items (one per tensor, after the chunks) check the headers of streams that
 // have no chunks; an empty batch gets one item that checks its header and table.
 #include "zvc_internal.cuh"
@@ -36,7 +36,8 @@ struct DecompressArgs {
   uint32_t batched;
   uint32_t warps_per_cta;
   uint32_t buf_words;          // largest valid chunk: C/32 masks + C words
-  uint32_t warp_stride_words;  // shared memory per warp: chunk (+3 for its phase), offsets, masks
+  uint32_t meta_offset_words;  // per window (position of its first value, mask), 8-byte aligned
+  uint32_t warp_stride_words;  // shared memory per warp: chunk (+3 for its phase), window table
   uint32_t* out[MAXT];
   uint64_t n[MAXT];
   uint64_t chunk_begin[MAXT + 1];
@@ -54,11 +55,9 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
   if (item >= a.total_items) return;
   Control* ctl = reinterpret_cast<Control*>(a.ws);
   const uint32_t C = a.chunk_elems;
-  const uint32_t wpc = C / kWindow;
   uint64_t* bar = reinterpret_cast<uint64_t*>(dsm) + warp;
   uint32_t* buf = dsm + kBarrierWords + (uint64_t)warp * a.warp_stride_words;
-  uint32_t* woffs = buf + a.buf_words + 4;
-  uint32_t* wmasks = woffs + wpc;
+  uint2* wmeta = reinterpret_cast<uint2*>(buf + a.meta_offset_words);  // (first value, mask)
 
   const bool is_chunk = item < a.total_chunks;
   uint32_t ti = 0;
@@ -79,19 +78,28 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
   const uint64_t n = ti < a.T ? a.n[ti] : 0;
   const uint64_t nc = ceil_div_u64(n, C);
 
-  // ---- locate and validate the stream (all lanes compute the same values)
+  // ---- locate and validate the stream (all lanes compute the same values). Every
+  // address read here is in bounds by sizes known before the round's loads, so each
+  // round issues all its loads at once: the batch table, then the stream header and the
+  // chunk's table entries.
   bool ok = true;
   uint64_t sb = 0, se = a.in_bytes;
   if (a.batched) {
     const uint64_t pre = 16 + 8 * ((uint64_t)a.T + 1);
-    ok = a.in_bytes >= pre && a.in[0] == kBatchMagic && a.in[1] == a.T &&
-         get_u64_words(a.in + 2) == a.in_bytes &&
-         get_u64_words(a.in + kBatchHeaderWords) == pre &&
-         get_u64_words(a.in + kBatchHeaderWords + 2 * (uint64_t)a.T) == a.in_bytes;
-    if (ok && ti < a.T) {
-      sb = get_u64_words(a.in + kBatchHeaderWords + 2 * (uint64_t)ti);
-      se = get_u64_words(a.in + kBatchHeaderWords + 2 * (uint64_t)ti + 2);
-      ok = sb <= se && se <= a.in_bytes && ((sb | se) & 3u) == 0;
+    if (a.in_bytes < pre) {
+      ok = false;
+    } else {
+      const uint32_t* bt = a.in + kBatchHeaderWords;
+      const uint32_t magic = a.in[0], t = a.in[1];
+      const uint64_t total = get_u64_words(a.in + 2);
+      const uint64_t first = get_u64_words(bt), last = get_u64_words(bt + 2 * (uint64_t)a.T);
+      if (ti < a.T) {
+        sb = get_u64_words(bt + 2 * (uint64_t)ti);
+        se = get_u64_words(bt + 2 * (uint64_t)ti + 2);
+      }
+      ok = (magic == kBatchMagic) & (t == a.T) & (total == a.in_bytes) & (first == pre) &
+           (last == a.in_bytes);
+      if (ti < a.T) ok = ok & (sb <= se) & (se <= a.in_bytes) & (((sb | se) & 3u) == 0);
     }
   }
   if (ti >= a.T) {  // empty batch: only its header and table exist
@@ -100,26 +108,33 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
   }
   const uint64_t table_end = 32 + 8 * nc;
   ok = ok && se - sb >= table_end;
-  const uint32_t* sw = a.in + sb / 4;
-  const uint64_t payload = ok ? (se - sb) - table_end : 0;
-  ok = ok && sw[0] == kStreamMagic && sw[1] == kVersionWordBytes && sw[2] == kWindow &&
-       sw[3] == C && get_u64_words(sw + 4) == n && get_u64_words(sw + 6) == payload;
-  if (!is_chunk) {
-    if (!ok && lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, item);
-    return;
-  }
-  const uint64_t cbeg = c * C;
-  const uint32_t count = (uint32_t)min((uint64_t)C, n - cbeg);
-  const uint32_t nwin = (count + kWindow - 1) / kWindow;
-  uint64_t start = 0, end = 0;
-  if (ok) {
-    start = get_u64_words(sw + kStreamHeaderWords + 2 * c);
-    end = (c + 1 < nc) ? get_u64_words(sw + kStreamHeaderWords + 2 * c + 2) : payload;
-    ok = (c != 0 || start == 0) && start <= end && end <= payload && ((start | end) & 3u) == 0 &&
-         (end - start) / 4 >= nwin && (end - start) / 4 <= (uint64_t)nwin + count;
-  }
   if (!ok) {
     if (lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, item);
+    return;
+  }
+  const uint32_t* sw = a.in + sb / 4;
+  const uint64_t payload = (se - sb) - table_end;
+  uint32_t h[kStreamHeaderWords];
+#pragma unroll
+  for (uint32_t j = 0; j < kStreamHeaderWords; ++j) h[j] = sw[j];
+  const uint64_t cbeg = c * C;
+  const uint32_t count = is_chunk ? (uint32_t)min((uint64_t)C, n - cbeg) : 0u;
+  const uint32_t nwin = (count + kWindow - 1) / kWindow;
+  uint64_t start = 0, end = payload;
+  if (is_chunk) {
+    const uint32_t* ct = sw + kStreamHeaderWords + 2 * c;
+    start = get_u64_words(ct);
+    if (c + 1 < nc) end = get_u64_words(ct + 2);
+  }
+  ok = (h[0] == kStreamMagic) & (h[1] == kVersionWordBytes) & (h[2] == kWindow) & (h[3] == C) &
+       (((uint64_t)h[4] | ((uint64_t)h[5] << 32)) == n) &
+       (((uint64_t)h[6] | ((uint64_t)h[7] << 32)) == payload);
+  if (is_chunk)
+    ok = ok & ((c != 0) | (start == 0)) & (start <= end) & (end <= payload) &
+         (((start | end) & 3u) == 0) && (end - start) / 4 >= nwin &&
+         (end - start) / 4 <= (uint64_t)nwin + count;
+  if (!ok || !is_chunk) {
+    if (!ok && lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, item);
     return;
   }
 
@@ -150,20 +165,22 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
   }
   __syncwarp();
 
-  // ---- walk the masks
+  // ---- walk the masks. The chain position -> mask -> next position is the critical
+  // path, so the loop carries nothing else: a window spans at most 33 words, so the k-th
+  // read sits below 33k <= buf_words - 33 and stays in this warp's buffer even for a
+  // corrupt chunk, and since positions only grow, ending exactly at len proves that every
+  // read was inside the chunk.
   uint32_t good = 1;
   if (lane == 0) {
-    uint32_t p = 0;
+    uint32_t pos = 0, m = 0;
+#pragma unroll 4
     for (uint32_t w = 0; w < nwin; ++w) {
-      if (p >= len) { good = 0; break; }
-      const uint32_t m = buf[p];
-      woffs[w] = p;
-      wmasks[w] = m;
-      p += 1u + __popc(m);
+      m = buf[pos];
+      wmeta[w] = make_uint2(pos + 1u, m);
+      pos += 1u + __popc(m);
     }
-    if (good && p != len) good = 0;
-    const uint32_t tail = count & (kWindow - 1);
-    if (good && tail != 0 && (wmasks[nwin - 1] >> tail) != 0u) good = 0;
+    const uint32_t ragged = count & (kWindow - 1);
+    good = (pos == len) & (ragged == 0 || (m >> ragged) == 0u);
   }
   good = __shfl_sync(0xffffffffu, good, 0);
   if (!good) {
@@ -172,26 +189,42 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
   }
   __syncwarp();
 
-  // ---- scatter
+  // ---- scatter: lane l expands words e .. e+3 (e = 4(l mod 8)) of windows l/8 + 4k;
+  // four windows per lane are in flight at once
   uint32_t* dst = a.out[ti] + cbeg;
   const bool vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
   const uint32_t e = 4u * (lane & 7u);
-  for (uint32_t w = lane >> 3; w < nwin; w += 4) {
-    const uint32_t m = wmasks[w];
-    const uint32_t o = woffs[w] + 1u;
-    uint32_t r[4];
+  const uint32_t below = (1u << e) - 1u;
+  for (uint32_t w0 = lane >> 3; w0 < nwin; w0 += 16) {
+    uint4 r[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t b = e + j;
-      r[j] = ((m >> b) & 1u) ? buf[o + __popc(m & ((1u << b) - 1u))] : 0u;
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w = w0 + 4u * k;
+      const uint2 mo = w < nwin ? wmeta[w] : make_uint2(0u, 0u);
+      const uint32_t m = mo.y;
+      uint32_t q = mo.x + __popc(m & below);
+      uint32_t v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t bit = (m >> (e + j)) & 1u;
+        v[j] = bit ? buf[q] : 0u;
+        q += bit;
+      }
+      r[k] = make_uint4(v[0], v[1], v[2], v[3]);
     }
-    const uint32_t base = w * kWindow + e;
-    if (vec && base + 4u <= count) {
-      *reinterpret_cast<uint4*>(dst + base) = make_uint4(r[0], r[1], r[2], r[3]);
-    } else {
 #pragma unroll
-      for (uint32_t j = 0; j < 4; ++j)
-        if (base + j < count) dst[base + j] = r[j];
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w = w0 + 4u * k;
+      const uint32_t base = w * kWindow + e;
+      if (w >= nwin) break;
+      if (vec && base + 4u <= count) {
+        *reinterpret_cast<uint4*>(dst + base) = r[k];
+      } else {
+        const uint32_t vv[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j)
+          if (base + j < count) dst[base + j] = vv[j];
+      }
     }
   }
 }
@@ -218,7 +251,8 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   args.total_items = chunks + (batched && T == 0 ? 1 : T);
   const uint32_t wpc = C / kWindow;
   args.buf_words = wpc + C;
-  args.warp_stride_words = (uint32_t)round_up_u64(args.buf_words + 4 + 2ull * wpc, 4);
+  args.meta_offset_words = (uint32_t)round_up_u64(args.buf_words + 4, 2);
+  args.warp_stride_words = (uint32_t)round_up_u64(args.meta_offset_words + 2ull * wpc, 4);
   const uint64_t per_warp = 4ull * args.warp_stride_words;
   uint32_t warps = (uint32_t)(73728ull / per_warp);
   warps = warps < 1 ? 1 : (warps > 8 ? 8 : warps);

@@ -358,21 +358,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
+// Suspend hint for mbarrier.try_wait: a waiting thread sleeps until the phase completes
+// or this many nanoseconds pass, so a warp that waits long does not spin on the issue slots.
+constexpr uint32_t kMbarSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "n"(kMbarSuspendNs)
       : "memory");
   return done != 0;
 }
 
 // Waits for the phase with the given parity to complete; false after limit_ns. try_wait
-// itself suspends the thread in hardware until the phase completes or a short internal
-// limit passes, so the loop only re-polls and checks the clock: no sleep that would delay
-// the wake-up.
+// itself suspends the thread in hardware until the phase completes or the suspend hint
+// passes, so the loop only re-polls and checks the clock: no sleep that would delay the
+// wake-up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = globaltimer_ns();

@@ -478,8 +478,9 @@ def measure_e2e(args, zvc, torch, xs, ns, C, dev, stream, step, hsize):
 
 
 def run_profile_case(args):
-    """Two warm-up launches then three measured launches of one kernel on AlexNet layer 0
-    (batch 128 x 96 x 55 x 55 fp32, 60% non-zero); prints their CUDA-event times."""
+    """Warm-up launches, then three timed groups of ten back-to-back launches of one kernel
+    on AlexNet layer 0 (batch 128 x 96 x 55 x 55 fp32, 60% non-zero); prints the mean
+    CUDA-event time per launch of each group."""
     import torch
 
     from activation_sparsity_compression_gb300 import build as zbuild
@@ -509,14 +510,18 @@ def run_profile_case(args):
         def launch():
             zvc.zvc_decompress(out.data_ptr(), S, y.data_ptr(), n, C, ws.data_ptr(), ws.numel(), sh)
     launch()
+    # launches are queued back to back, so the device never waits for the host between
+    # them; each entry is the mean over a group of `reps` launches
+    reps = 10
     times = []
     for _ in range(4):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        launch()
+        for _ in range(reps):
+            launch()
         e1.record()
         torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
+        times.append(e0.elapsed_time(e1) / reps)
     assert zvc.zvc_get_error(ws.data_ptr(), sh) == zvc.ZVC_OK
     if args.profile == "decompress":
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))

@@ -151,7 +151,11 @@ uint64_t zvc_offload_workspace_size(uint64_t n, uint32_t chunk_elems);
  * BLOCKS the calling thread until the last segment's copy has been enqueued (the host
  * must learn each compressed size before it can enqueue the copy); the copies complete
  * in `stream` order, and *h_size (host) holds the batch's byte count on return.
- * h_cap >= zvc_offload_host_bound(n, C). h_pinned must be page-locked. */
+ * h_cap >= zvc_offload_host_bound(n, C). h_pinned must be page-locked (cudaHostAlloc,
+ * cudaMallocHost or cudaHostRegister), hence mapped into the device's address space
+ * under unified addressing, and 8-byte aligned: the compress kernels store each
+ * segment's size straight into the buffer's batch table. Other host memory returns
+ * ZVC_ERR_INVALID_ARG. */
 zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void* h_pinned,
                        uint64_t h_cap, uint64_t* h_size, void* d_ws, uint64_t ws_bytes,
                        void* stream);
