@@ -57,6 +57,7 @@ _SIGS = {
     "zvc_offload_segment_elems": (_u64, [_u64, _u32]),
     "zvc_offload_host_bound": (_u64, [_u64, _u32]),
     "zvc_offload_workspace_size": (_u64, [_u64, _u32]),
+    "zvc_offload_join": (_st, [_vp]),
     "zvc_offload": (_st, [_vp, _u64, _u32, _vp, _u64, ctypes.POINTER(_u64), _vp, _u64, _vp]),
     "zvc_prefetch": (_st, [_vp, _u64, _vp, _u64, _u32, _vp, _u64, _vp]),
     "zvc_selftest_wait_timeout": (_st, [_vp, _u64, _u64, _vp]),
@@ -174,6 +175,11 @@ def zvc_offload(d_in, n, chunk_elems, h_pinned, h_cap, d_ws, ws_bytes, stream):
     st = int(lib().zvc_offload(d_in, n, chunk_elems, h_pinned, h_cap, ctypes.byref(size), d_ws,
                                ws_bytes, stream))
     return st, int(size.value)
+
+
+def zvc_offload_join(stream):
+    """Work enqueued on `stream` afterwards waits for every copy zvc_offload enqueued."""
+    return int(lib().zvc_offload_join(stream))
 
 
 def zvc_prefetch(h_pinned, h_size, d_out, n, chunk_elems, d_ws, ws_bytes, stream):

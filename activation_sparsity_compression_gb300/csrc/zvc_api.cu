@@ -53,12 +53,13 @@ struct SegPlan {
 };
 
 uint64_t segment_elems(uint64_t n, uint32_t c) {
-  // About eight segments per tensor, each between 4 MiB and 64 MiB of words, so the copy
-  // of one segment overlaps the compression of the next; whole chunks only.
-  uint64_t s = ceil_div_u64(n, 8);
-  if (s < (1ull << 20)) s = 1ull << 20;
-  if (s > (1ull << 24)) s = 1ull << 24;
-  return round_up_u64(s, c);
+  // Equal segments of at most about 4 Mi words (16 MiB of fp32), whole chunks: a
+  // segment's compressed copy (several MB) is long against the ~2 us fixed cost of a
+  // copy and against the compression of the next segment, and one tensor's last copies
+  // overlap the next tensor's compression.
+  constexpr uint64_t kTarget = 1ull << 22;
+  const uint64_t count = n == 0 ? 1 : ceil_div_u64(n, kTarget);
+  return round_up_u64(ceil_div_u64(n == 0 ? 1 : n, count), c);
 }
 
 SegPlan seg_plan(uint64_t n, uint32_t c) {
@@ -78,7 +79,7 @@ struct Pipe {
   cudaStream_t side = nullptr;
   cudaEvent_t kernel_done[kPipeDepth];
   cudaEvent_t copy_done[kPipeDepth];
-  cudaEvent_t start = nullptr;
+  cudaEvent_t joined = nullptr;
   std::mutex mu;
 };
 
@@ -101,7 +102,7 @@ zvc_status get_pipe(Pipe** out) {
     e = cudaEventCreateWithFlags(&p->kernel_done[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done[i], cudaEventDisableTiming);
   }
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->start, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->joined, cudaEventDisableTiming);
   if (e != cudaSuccess) return cuda_failure(e);  // the partial set leaks; CUDA is unusable
   g_pipes[dev] = p;
   *out = p;
@@ -357,7 +358,9 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
 
   for (uint64_t k = 0; k < S; ++k) {
     const int b = (int)(k % kPipeDepth);
-    if (k >= (uint64_t)kPipeDepth) ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
+    // staging buffer b is free once the copy that last read it (this call's or an
+    // earlier one's) is done
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
     const uint64_t nk = (k + 1 < S) ? p.seg : n - k * p.seg;
     const TensorIn t{in + k * p.seg, nk};
     *reinterpret_cast<volatile uint64_t*>(H + 16 + 8 * k) = 0;
@@ -376,9 +379,17 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
   put_u32(H + 4, (uint32_t)S);
   put_u64(H + 8, pos);
   for (uint64_t k = 0; k <= S; ++k) put_u64(H + 16 + 8 * k, offs[k]);
-  for (uint64_t b = 0; b < S && b < (uint64_t)kPipeDepth; ++b)
-    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
   *h_size = pos;
+  return ZVC_OK;
+}
+
+zvc_status zvc_offload_join(void* stream) {
+  Pipe* pipe = nullptr;
+  zvc_status st = get_pipe(&pipe);
+  if (st != ZVC_OK) return st;
+  std::lock_guard<std::mutex> lk(pipe->mu);
+  ZVC_CUDA_TRY(cudaEventRecord(pipe->joined, pipe->side));
+  ZVC_CUDA_TRY(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), pipe->joined, 0));
   return ZVC_OK;
 }
 
@@ -410,14 +421,14 @@ zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
   uint32_t* out = static_cast<uint32_t*>(d_out);
-  // copies start after work already enqueued on `stream` (e.g. an offload's copies)
-  ZVC_CUDA_TRY(cudaEventRecord(pipe->start, s));
-  ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->start, 0));
+  // The copies run on the library's copy stream, after its earlier copies (an offload's,
+  // which wrote h_pinned); staging buffer b is free once the kernel that last read or
+  // wrote it is done.
   for (uint64_t k = 0; k < S; ++k) {
     const int b = (int)(k % kPipeDepth);
     const uint64_t a = get_u64(H + 16 + 8 * k), sz = get_u64(H + 24 + 8 * k) - a;
     uint8_t* stage = ws + p.stage_off + b * p.stage;
-    if (k >= (uint64_t)kPipeDepth) ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->kernel_done[b], 0));
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->kernel_done[b], 0));
     ZVC_CUDA_TRY(cudaMemcpyAsync(stage, H + a, sz, cudaMemcpyHostToDevice, pipe->side));
     ZVC_CUDA_TRY(cudaEventRecord(pipe->copy_done[b], pipe->side));
     ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));

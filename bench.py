@@ -410,6 +410,7 @@ def measure_components(args, zvc, torch, xs, ns, C, dev, stream, peak):
         for l in range(len(ns)):
             _, hs[l] = zvc.zvc_offload(xs[l].data_ptr(), ns[l], C, hb[l].data_ptr(), hcap[l],
                                        ows[l].data_ptr(), ows[l].numel(), sh)
+    zvc.zvc_offload_join(sh)  # the offload is done when its copies are
     ev[1].record(stream)
     for _ in range(reps):
         for l in range(len(ns)):

@@ -130,8 +130,9 @@ zvc_status zvc_decompress_batched(const void* d_in, uint64_t in_bytes, void* con
                                   const uint64_t* ns, uint32_t T, uint32_t chunk_elems,
                                   void* d_ws, uint64_t ws_bytes, void* stream);
 
-/* Segment length (words) that zvc_offload uses for a tensor of n words: a whole number
- * of chunks, about 16 Mi words (64 MiB of fp32). */
+/* Segment length (words) that zvc_offload uses for a tensor of n words: n cut into
+ * ceil(n / 2^22) equal parts, rounded up to whole chunks (at most about 4 Mi words,
+ * 16 MiB of fp32). */
 uint64_t zvc_offload_segment_elems(uint64_t n, uint32_t chunk_elems);
 
 /* Host bytes zvc_offload may need: the batch bound over its segments. */
@@ -145,12 +146,18 @@ uint64_t zvc_offload_workspace_size(uint64_t n, uint32_t chunk_elems);
  * cudaMemcpyAsync, cDMA compresses them on the way). The tensor is cut into segments
  * of zvc_offload_segment_elems() words; each segment is compressed on `stream` into a
  * device staging buffer and copied to the pinned host buffer h_pinned with
- * cudaMemcpyAsync on a side stream, so the copy of segment k overlaps the compression
- * of segment k+1. h_pinned receives a batch (format above) whose streams are the
- * segments; it is byte-identical to zvc_compress_batched over the segments.
- * BLOCKS the calling thread until the last segment's copy has been enqueued (the host
- * must learn each compressed size before it can enqueue the copy); the copies complete
- * in `stream` order, and *h_size (host) holds the batch's byte count on return.
+ * cudaMemcpyAsync on the library's copy stream (one per device), so the copy of segment
+ * k overlaps the compression of segment k+1, and the compression of the next tensor
+ * overlaps the copies of this one. h_pinned receives a batch (format above) whose
+ * streams are the segments; it is byte-identical to zvc_compress_batched over the
+ * segments.
+ * BLOCKS the calling thread until the last segment is compressed and its copy enqueued
+ * (the host must learn each compressed size before it can enqueue the copy); *h_size
+ * (host) holds the batch's byte count on return. Work enqueued on `stream` afterwards
+ * waits for the compression only, not for the copies: d_in may be overwritten then,
+ * h_pinned is complete once zvc_offload_join() has joined the copies into a stream
+ * and that stream has reached that point (or the device is synchronised). A
+ * zvc_prefetch of the batch needs no join: its copies follow on the same copy stream.
  * h_cap >= zvc_offload_host_bound(n, C). h_pinned must be page-locked (cudaHostAlloc,
  * cudaMallocHost or cudaHostRegister), hence mapped into the device's address space
  * under unified addressing, and 8-byte aligned: the compress kernels store each
@@ -160,13 +167,21 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
                        uint64_t h_cap, uint64_t* h_size, void* d_ws, uint64_t ws_bytes,
                        void* stream);
 
+/* Offload join: work enqueued on `stream` after this call waits for every copy that
+ * zvc_offload has enqueued on this device so far. */
+zvc_status zvc_offload_join(void* stream);
+
 /* Prefetch (section V.D: vDNN prefetches offloaded activations before backward
  * propagation): copies each segment stream of the batch in h_pinned (h_size bytes, as
  * written by zvc_offload for n words and chunk_elems C) to device staging with
- * cudaMemcpyAsync on a side stream and decompresses it into d_out on `stream`, the copy
- * of segment k+1 overlapping the decompression of segment k. Reads the batch table on
- * the host (a malformed table returns ZVC_ERR_CORRUPT at once); device-side corruption
- * is latched as for zvc_decompress. Does not block the calling thread. */
+ * cudaMemcpyAsync on the library's copy stream and decompresses it into d_out on
+ * `stream`, the copy of segment k+1 overlapping the decompression of segment k. The
+ * copies follow the library's earlier copies (so an offload of h_pinned completes
+ * first) and the kernel that last used each staging buffer; they do not wait for other
+ * work on `stream`: a caller that fills h_pinned through `stream` synchronises first.
+ * Reads the batch table on the host (a malformed table returns ZVC_ERR_CORRUPT at
+ * once); device-side corruption is latched as for zvc_decompress. Does not block the
+ * calling thread. */
 zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint64_t n,
                         uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream);
 

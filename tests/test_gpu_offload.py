@@ -80,3 +80,36 @@ def test_prefetch_latches_corrupt_segment():
     assert zvc.zvc_prefetch(bad.data_ptr(), size, y.data_ptr(), n, C, ws.data_ptr(), ws.numel(),
                             sh()) == zvc.ZVC_OK
     assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_ERR_CORRUPT
+
+
+def test_offload_join_makes_the_host_batch_complete_on_the_callers_stream():
+    ensure_lib()
+    n, C = 5_000_000, 4096
+    x = workloads.odd_case(n, device="cuda", density=0.4)[0]
+    cap = zvc.zvc_offload_host_bound(n, C)
+    h = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+    ws = zvc.new_workspace(zvc.zvc_offload_workspace_size(n, C))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    st, size = zvc.zvc_offload(x.data_ptr(), n, C, h.data_ptr(), cap, ws.data_ptr(), ws.numel(),
+                               s.cuda_stream)
+    assert st == zvc.ZVC_OK
+    assert zvc.zvc_offload_join(s.cuda_stream) == zvc.ZVC_OK
+    s.synchronize()  # this stream only: the join put the copies on it
+    seg = zvc.zvc_offload_segment_elems(n, C)
+    w = words_of(x)
+    ref = oracle.encode_batch([w[k:k + seg] for k in range(0, n, seg)], C)
+    assert size == ref.size
+    assert np.array_equal(h[:size].numpy(), ref)
+
+
+def test_offload_rejects_a_host_buffer_off_8_byte_alignment():
+    ensure_lib()
+    n, C = 100_000, 4096
+    x = workloads.odd_case(n, device="cuda")[0]
+    cap = zvc.zvc_offload_host_bound(n, C)
+    h = torch.empty(cap + 8, dtype=torch.uint8, pin_memory=True)
+    ws = zvc.new_workspace(zvc.zvc_offload_workspace_size(n, C))
+    st, _ = zvc.zvc_offload(x.data_ptr(), n, C, h.data_ptr() + 4, cap, ws.data_ptr(), ws.numel(),
+                            sh())
+    assert st == zvc.ZVC_ERR_INVALID_ARG
