@@ -53,11 +53,12 @@ struct SegPlan {
 };
 
 uint64_t segment_elems(uint64_t n, uint32_t c) {
-  // Equal segments of at most about 4 Mi words (16 MiB of fp32), whole chunks: a
-  // segment's compressed copy (several MB) is long against the ~2 us fixed cost of a
-  // copy and against the compression of the next segment, and one tensor's last copies
-  // overlap the next tensor's compression.
-  constexpr uint64_t kTarget = 1ull << 22;
+  // Equal segments of at most about 16 Mi words (64 MiB of fp32), whole chunks. Within a
+  // tensor the copy of one segment overlaps the compression of the next; across tensors
+  // the copies of one overlap the compression of the next, so only the first segment's
+  // compression and the last one's decompression are exposed, and both kernels run on
+  // tens of MB per launch.
+  constexpr uint64_t kTarget = 1ull << 24;
   const uint64_t count = n == 0 ? 1 : ceil_div_u64(n, kTarget);
   return round_up_u64(ceil_div_u64(n == 0 ? 1 : n, count), c);
 }
