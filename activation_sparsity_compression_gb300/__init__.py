@@ -57,6 +57,7 @@ _SIGS = {
     "zvc_offload_segment_elems": (_u64, [_u64, _u32]),
     "zvc_offload_host_bound": (_u64, [_u64, _u32]),
     "zvc_offload_workspace_size": (_u64, [_u64, _u32]),
+    "zvc_compress_static_get_error": (_st, [_vp]),
     "zvc_offload_join": (_st, [_vp]),
     "zvc_offload": (_st, [_vp, _u64, _u32, _vp, _u64, ctypes.POINTER(_u64), _vp, _u64, _vp]),
     "zvc_prefetch": (_st, [_vp, _u64, _vp, _u64, _u32, _vp, _u64, _vp]),
@@ -138,6 +139,11 @@ def zvc_compress_static(d_in, n, chunk_elems, d_out, out_cap, d_out_size, stream
     """zvc_compress for callers that cannot allocate device memory: no workspace, the
     scratch is a static device array inside the library (n <= ZVC_STATIC_MAX_ELEMS)."""
     return int(lib().zvc_compress_static(d_in, n, chunk_elems, d_out, out_cap, d_out_size, stream))
+
+
+def zvc_compress_static_get_error(stream):
+    """Status latched by zvc_compress_static on this device since the last read; clears it."""
+    return int(lib().zvc_compress_static_get_error(stream))
 
 
 def zvc_decompress(d_in, in_bytes, d_out, n, chunk_elems, d_ws, ws_bytes, stream):

@@ -10,9 +10,10 @@
 // kStaticScratchBytes of it until the process exits.
 //
 // The array is shared by every call on a device and keeps the previous call's contents;
-// each call clears the parts that must start at zero before its kernel runs. Two calls
-// whose work overlaps on the GPU (different streams, no ordering between them) use the
-// same scratch and race: order them on one stream or synchronise between them.
+// each call clears the parts that must start at zero before its kernel runs, except the
+// error latch, which keeps a failure until zvc_compress_static_get_error reads it. Two
+// calls whose work overlaps on the GPU (different streams, no ordering between them) use
+// the same scratch and race: order them on one stream or synchronise between them.
 #include <mutex>
 
 #include "zvc_internal.cuh"
@@ -70,11 +71,14 @@ extern "C" zvc_status zvc_compress_static(const void* d_in, uint64_t n, uint32_t
   zvc_status st = scratch_for_current_device(&scratch);
   if (st != ZVC_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // nobody reads this scratch's error word: forget the previous call's, so that a
-  // failure shows only as *d_out_size == 0
-  cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(zvc::Control), s);
-  if (e != cudaSuccess) return zvc::cuda_failure(e);
   const zvc::TensorIn t{static_cast<const uint32_t*>(d_in), n};
   return zvc::launch_compress(&t, 1, false, chunk_elems, static_cast<uint32_t*>(d_out),
                               out_cap / 4, d_out_size, scratch, zvc::kDefaultWaitLimitNs, s);
+}
+
+extern "C" zvc_status zvc_compress_static_get_error(void* stream) {
+  uint8_t* scratch = nullptr;
+  zvc_status st = scratch_for_current_device(&scratch);
+  if (st != ZVC_OK) return st;
+  return zvc_get_error(scratch, stream);
 }

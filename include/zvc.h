@@ -99,14 +99,18 @@ zvc_status zvc_compress(const void* d_in, uint64_t n, uint32_t chunk_elems, void
  * scratch is one static device array of about 1 MiB that every GPU loading the library
  * keeps until exit. Limits: n <= ZVC_STATIC_MAX_ELEMS, else ZVC_ERR_INVALID_ARG. The
  * first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * and caches it; make that first call before any stream capture. The call allocates
- * nothing. All calls on a device share the array and clear it as they start, so calls
- * whose GPU work overlaps (unordered streams) race and must be ordered by the caller.
- * A failure on the device leaves *d_out_size == 0 (a valid stream has at least 32 bytes);
- * there is no workspace to read an error code from. */
+ * and caches it. The call allocates nothing. All calls on a device share the array, so
+ * calls whose GPU work overlaps (unordered streams) race and must be ordered by the
+ * caller. A failure on the device (a wait that gave up) is latched in the array, where
+ * it stays until zvc_compress_static_get_error() reads it; the stream's bytes and
+ * *d_out_size are then unspecified. */
 #define ZVC_STATIC_MAX_ELEMS (1ull << 29) /* 2 GiB of 4-byte words */
 zvc_status zvc_compress_static(const void* d_in, uint64_t n, uint32_t chunk_elems, void* d_out,
                                uint64_t out_cap, uint64_t* d_out_size, void* stream);
+
+/* The status latched by zvc_compress_static calls on the current device since the last
+ * read (ZVC_OK if none): synchronises `stream`, reads the latch and clears it. */
+zvc_status zvc_compress_static_get_error(void* stream);
 
 /* Decompress the stream of in_bytes bytes at d_in into n words at d_out (inverse of
  * section V.A: a set mask bit takes the next packed word, a clear bit writes zero).

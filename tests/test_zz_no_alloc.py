@@ -25,7 +25,7 @@ def _static_compress(x, C):
     size = torch.zeros(1, dtype=torch.int64, device=x.device)
     st = zvc.zvc_compress_static(x.data_ptr(), n, C, out.data_ptr(), cap, size.data_ptr(), sh())
     assert st == zvc.ZVC_OK
-    torch.cuda.synchronize()
+    assert zvc.zvc_compress_static_get_error(sh()) == zvc.ZVC_OK  # nothing latched
     s = int(size.item())
     host = out.cpu().numpy()
     assert (host[s:] == 0xEE).all()  # nothing written past the stream
