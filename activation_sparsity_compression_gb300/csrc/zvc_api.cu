@@ -42,14 +42,18 @@ void put_u64(uint8_t* p, uint64_t v) { std::memcpy(p, &v, 8); }
 uint32_t get_u32(const uint8_t* p) { uint32_t v; std::memcpy(&v, p, 4); return v; }
 uint64_t get_u64(const uint8_t* p) { uint64_t v; std::memcpy(&v, p, 8); return v; }
 
+#define ZVC_CUDA_TRY(expr)                          \
+  do {                                              \
+    const cudaError_t e_ = (expr);                  \
+    if (e_ != cudaSuccess) return cuda_failure(e_); \
+  } while (0)
+
 // ---------------------------------------------------------------- offload plan
 struct SegPlan {
   uint64_t seg;         // words per segment (whole chunks)
   uint64_t count;       // segments
-  uint64_t kernel_ws;   // workspace bytes for one segment's compress
-  uint64_t stage;       // bytes of one staging buffer
-  uint64_t stage_off;   // offset of staging buffer 0
-  uint64_t total;       // workspace bytes
+  uint64_t kernel_ws;   // workspace bytes one segment's compress needs
+  uint64_t stage;       // bytes one staging buffer needs
 };
 
 uint64_t segment_elems(uint64_t n, uint32_t c) {
@@ -70,17 +74,44 @@ SegPlan seg_plan(uint64_t n, uint32_t c) {
   const uint64_t seg_n = n < p.seg ? n : p.seg;
   p.kernel_ws = compress_ws_bytes(tiles_for(seg_n), 1);
   p.stage = round_up_u64(stream_bound(seg_n, c), ZVC_WORKSPACE_ALIGN);
-  p.stage_off = round_up_u64(p.kernel_ws, ZVC_WORKSPACE_ALIGN);
-  p.total = p.stage_off + kPipeDepth * p.stage;
   return p;
 }
 
-// Side stream and events for the pipeline, one set per device, created on first use.
-struct Pipe {
-  cudaStream_t side = nullptr;
+// Where an offload workspace keeps the compress kernel's area and its three staging
+// buffers. It depends on the workspace's size alone, so every offload and prefetch through
+// one workspace, whatever its tensor's size, puts staging buffer b at the same bytes, and
+// the per-buffer events of that workspace order every use of them.
+struct WsLayout {
+  uint64_t kernel_ws;  // bytes [0, kernel_ws): the compress kernel's area
+  uint64_t stage;      // staging buffer b at kernel_ws + b * stage
+};
+
+WsLayout ws_layout(uint64_t ws_bytes) {
+  WsLayout l;
+  const uint64_t k = ceil_div_u64(ws_bytes, 1024);
+  l.kernel_ws = round_up_u64(k < 4096 ? 4096 : k, ZVC_WORKSPACE_ALIGN);
+  l.stage = ws_bytes > l.kernel_ws
+                ? (ws_bytes - l.kernel_ws) / kPipeDepth / ZVC_WORKSPACE_ALIGN * ZVC_WORKSPACE_ALIGN
+                : 0;
+  return l;
+}
+
+bool layout_fits(const WsLayout& l, const SegPlan& p) {
+  return l.kernel_ws >= p.kernel_ws && l.stage >= p.stage;
+}
+
+// Side stream (the copy stream) for the pipeline, one per device, created on first use,
+// and per workspace the events of its staging buffers: the kernel and the copy that last
+// used buffer b.
+struct Slots {
   cudaEvent_t kernel_done[kPipeDepth];
   cudaEvent_t copy_done[kPipeDepth];
+};
+
+struct Pipe {
+  cudaStream_t side = nullptr;
   cudaEvent_t joined = nullptr;
+  std::map<uintptr_t, Slots> slots;  // by workspace address
   std::mutex mu;
 };
 
@@ -99,14 +130,38 @@ zvc_status get_pipe(Pipe** out) {
   }
   Pipe* p = new Pipe();
   e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
-  for (int i = 0; i < kPipeDepth && e == cudaSuccess; ++i) {
-    e = cudaEventCreateWithFlags(&p->kernel_done[i], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->copy_done[i], cudaEventDisableTiming);
-  }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->joined, cudaEventDisableTiming);
   if (e != cudaSuccess) return cuda_failure(e);  // the partial set leaks; CUDA is unusable
   g_pipes[dev] = p;
   *out = p;
+  return ZVC_OK;
+}
+
+// The staging-buffer events of workspace ws (created on first use). Called with pipe->mu
+// held. A process that cycles through very many workspaces drops the whole table once it
+// holds 4096 of them, after waiting for every event in it.
+zvc_status slots_for(Pipe* pipe, const void* ws, Slots** out) {
+  const uintptr_t key = reinterpret_cast<uintptr_t>(ws);
+  auto it = pipe->slots.find(key);
+  if (it == pipe->slots.end()) {
+    if (pipe->slots.size() >= 4096) {
+      for (auto& kv : pipe->slots)
+        for (int b = 0; b < kPipeDepth; ++b) {
+          ZVC_CUDA_TRY(cudaEventSynchronize(kv.second.kernel_done[b]));
+          ZVC_CUDA_TRY(cudaEventSynchronize(kv.second.copy_done[b]));
+          cudaEventDestroy(kv.second.kernel_done[b]);
+          cudaEventDestroy(kv.second.copy_done[b]);
+        }
+      pipe->slots.clear();
+    }
+    Slots sl;
+    for (int b = 0; b < kPipeDepth; ++b) {
+      ZVC_CUDA_TRY(cudaEventCreateWithFlags(&sl.kernel_done[b], cudaEventDisableTiming));
+      ZVC_CUDA_TRY(cudaEventCreateWithFlags(&sl.copy_done[b], cudaEventDisableTiming));
+    }
+    it = pipe->slots.emplace(key, sl).first;
+  }
+  *out = &it->second;
   return ZVC_OK;
 }
 
@@ -117,11 +172,6 @@ zvc_status read_latched(void* d_ws) {
   return err ? (zvc_status)err : ZVC_ERR_CUDA;
 }
 
-#define ZVC_CUDA_TRY(expr)                          \
-  do {                                              \
-    const cudaError_t e_ = (expr);                  \
-    if (e_ != cudaSuccess) return cuda_failure(e_); \
-  } while (0)
 
 // ---------------------------------------------------------------- tracing
 struct TraceRec {
@@ -301,7 +351,11 @@ uint64_t zvc_offload_host_bound(uint64_t n, uint32_t chunk_elems) {
 
 uint64_t zvc_offload_workspace_size(uint64_t n, uint32_t chunk_elems) {
   if (!chunk_ok(chunk_elems) || n > kMaxElems) return 0;
-  return seg_plan(n, chunk_elems).total;
+  const SegPlan p = seg_plan(n, chunk_elems);
+  // the smallest size whose layout fits: about kPipeDepth * stage + 1/1024 of itself
+  uint64_t w = round_up_u64(kPipeDepth * p.stage + p.kernel_ws + 4096, ZVC_WORKSPACE_ALIGN);
+  while (!layout_fits(ws_layout(w), p)) w += round_up_u64(w / 512 + 1, ZVC_WORKSPACE_ALIGN);
+  return w;
 }
 
 zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void* h_pinned,
@@ -313,7 +367,8 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
     return ZVC_ERR_INVALID_ARG;
   const SegPlan p = seg_plan(n, chunk_elems);
   if (p.count > UINT32_MAX) return ZVC_ERR_INVALID_ARG;
-  if (h_cap < zvc_offload_host_bound(n, chunk_elems) || ws_bytes < p.total)
+  const WsLayout L = ws_layout(ws_bytes);
+  if (h_cap < zvc_offload_host_bound(n, chunk_elems) || !layout_fits(L, p))
     return ZVC_ERR_BUFFER_TOO_SMALL;
   // The kernels store each segment's compressed size straight into the pinned buffer, so
   // the host learns it without a copy queued behind the previous segment's transfer.
@@ -329,6 +384,8 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
   zvc_status st = get_pipe(&pipe);
   if (st != ZVC_OK) return st;
   std::lock_guard<std::mutex> lk(pipe->mu);
+  Slots* sl = nullptr;
+  if ((st = slots_for(pipe, d_ws, &sl)) != ZVC_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
@@ -345,32 +402,33 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
   // host put there.
   auto enqueue_copy = [&](uint64_t k) -> zvc_status {
     const int b = (int)(k % kPipeDepth);
-    ZVC_CUDA_TRY(cudaEventSynchronize(pipe->kernel_done[b]));
+    ZVC_CUDA_TRY(cudaEventSynchronize(sl->kernel_done[b]));
     const uint64_t sz = *reinterpret_cast<volatile uint64_t*>(H + 16 + 8 * k);
-    if (sz == 0 || sz > p.stage || pos + sz > h_cap) return read_latched(d_ws);
+    if (sz == 0 || sz > L.stage || pos + sz > h_cap) return read_latched(d_ws);
     offs[k] = pos;
-    ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->kernel_done[b], 0));
-    ZVC_CUDA_TRY(cudaMemcpyAsync(H + pos, ws + p.stage_off + b * p.stage, sz,
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, sl->kernel_done[b], 0));
+    ZVC_CUDA_TRY(cudaMemcpyAsync(H + pos, ws + L.kernel_ws + b * L.stage, sz,
                                  cudaMemcpyDeviceToHost, pipe->side));
-    ZVC_CUDA_TRY(cudaEventRecord(pipe->copy_done[b], pipe->side));
+    ZVC_CUDA_TRY(cudaEventRecord(sl->copy_done[b], pipe->side));
     pos += sz;
     return ZVC_OK;
   };
 
   for (uint64_t k = 0; k < S; ++k) {
     const int b = (int)(k % kPipeDepth);
-    // staging buffer b is free once the copy that last read it (this call's or an
-    // earlier one's) is done
-    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
+    // staging buffer b is free once the copy and the kernel that last used it (this
+    // call's or an earlier one's, on any stream) are done
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, sl->copy_done[b], 0));
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, sl->kernel_done[b], 0));
     const uint64_t nk = (k + 1 < S) ? p.seg : n - k * p.seg;
     const TensorIn t{in + k * p.seg, nk};
     *reinterpret_cast<volatile uint64_t*>(H + 16 + 8 * k) = 0;
     st = launch_compress(&t, 1, false, chunk_elems,
-                         reinterpret_cast<uint32_t*>(ws + p.stage_off + b * p.stage), p.stage / 4,
+                         reinterpret_cast<uint32_t*>(ws + L.kernel_ws + b * L.stage), L.stage / 4,
                          reinterpret_cast<uint64_t*>(Hdev + 16 + 8 * k), ws, kDefaultWaitLimitNs,
                          s);
     if (st != ZVC_OK) return st;
-    ZVC_CUDA_TRY(cudaEventRecord(pipe->kernel_done[b], s));
+    ZVC_CUDA_TRY(cudaEventRecord(sl->kernel_done[b], s));
     if (k >= 1 && (st = enqueue_copy(k - 1)) != ZVC_OK) return st;
   }
   if (S >= 1 && (st = enqueue_copy(S - 1)) != ZVC_OK) return st;
@@ -400,7 +458,8 @@ zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint
       (n > 0 && d_out == nullptr) || !aligned(d_out, 4) || !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
     return ZVC_ERR_INVALID_ARG;
   const SegPlan p = seg_plan(n, chunk_elems);
-  if (ws_bytes < p.total) return ZVC_ERR_BUFFER_TOO_SMALL;
+  const WsLayout L = ws_layout(ws_bytes);
+  if (!layout_fits(L, p)) return ZVC_ERR_BUFFER_TOO_SMALL;
   const uint8_t* H = static_cast<const uint8_t*>(h_pinned);
   const uint64_t S = p.count;
   const uint64_t prefix = batch_prefix((uint32_t)S);
@@ -418,6 +477,8 @@ zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint
   zvc_status st = get_pipe(&pipe);
   if (st != ZVC_OK) return st;
   std::lock_guard<std::mutex> lk(pipe->mu);
+  Slots* sl = nullptr;
+  if ((st = slots_for(pipe, d_ws, &sl)) != ZVC_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
@@ -428,17 +489,17 @@ zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint
   for (uint64_t k = 0; k < S; ++k) {
     const int b = (int)(k % kPipeDepth);
     const uint64_t a = get_u64(H + 16 + 8 * k), sz = get_u64(H + 24 + 8 * k) - a;
-    uint8_t* stage = ws + p.stage_off + b * p.stage;
-    ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, pipe->kernel_done[b], 0));
+    uint8_t* stage = ws + L.kernel_ws + b * L.stage;
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, sl->kernel_done[b], 0));
     ZVC_CUDA_TRY(cudaMemcpyAsync(stage, H + a, sz, cudaMemcpyHostToDevice, pipe->side));
-    ZVC_CUDA_TRY(cudaEventRecord(pipe->copy_done[b], pipe->side));
-    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, pipe->copy_done[b], 0));
+    ZVC_CUDA_TRY(cudaEventRecord(sl->copy_done[b], pipe->side));
+    ZVC_CUDA_TRY(cudaStreamWaitEvent(s, sl->copy_done[b], 0));
     const uint64_t nk = (k + 1 < S) ? p.seg : n - k * p.seg;
     const TensorOut t{out + k * p.seg, nk};
     st = launch_decompress(reinterpret_cast<const uint32_t*>(stage), sz, &t, 1, false,
                            chunk_elems, ws, s);
     if (st != ZVC_OK) return st;
-    ZVC_CUDA_TRY(cudaEventRecord(pipe->kernel_done[b], s));
+    ZVC_CUDA_TRY(cudaEventRecord(sl->kernel_done[b], s));
   }
   return ZVC_OK;
 }

@@ -143,7 +143,10 @@ uint64_t zvc_offload_segment_elems(uint64_t n, uint32_t chunk_elems);
 uint64_t zvc_offload_host_bound(uint64_t n, uint32_t chunk_elems);
 
 /* Workspace bytes for zvc_offload / zvc_prefetch: device staging for the pipelined
- * segments plus the per-segment kernel workspace. */
+ * segments plus the per-segment kernel workspace. Where these sit inside a workspace
+ * depends on its size alone, so one workspace of W bytes serves, in any order and on any
+ * stream, every tensor whose zvc_offload_workspace_size is at most W; a smaller W returns
+ * ZVC_ERR_BUFFER_TOO_SMALL. */
 uint64_t zvc_offload_workspace_size(uint64_t n, uint32_t chunk_elems);
 
 /* Offload (section V.D: vDNN offloads activations during forward propagation with

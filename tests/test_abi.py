@@ -96,3 +96,9 @@ def test_product_code_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", text, re.M), f
                 assert "zvc_oracle" not in text and "zvco_" not in text, f
+
+
+def test_offload_hooks_reject_an_unknown_placement():
+    from activation_sparsity_compression_gb300.offload import ActivationOffload
+    with pytest.raises(ValueError):
+        ActivationOffload(where="disk")
