@@ -51,6 +51,10 @@ def parse_args(argv=None):
     p.add_argument("--profile", choices=["compress", "decompress"],
                    help="run a few launches of one kernel on AlexNet layer 0 (149 MB) and "
                         "exit: the small case for ncu captures")
+    p.add_argument("--train", action="store_true",
+                   help="training step of a VGG-style CNN with its saved activations kept, "
+                        "offloaded compressed to host memory, or kept compressed in HBM; "
+                        "prints one JSON line and exits")
     p.add_argument("--write-traffic", nargs=2, metavar=("COMPRESS_CSV", "DECOMPRESS_CSV"),
                    help="turn ncu DRAM counters of one step's launches (see TRAFFIC_FILE) "
                         "into that file, keyed by the kernels' source hashes, and exit")
@@ -612,10 +616,93 @@ def run_profile_case(args):
     return 0
 
 
+# ------------------------------------------------------------------ training step with offload
+TRAIN_MODEL = ("deep CNN: conv 3->128 (3x3, stride 2) + ReLU, then 12 x (conv 128->128 3x3 + "
+               "ReLU) at 112x112, global average pool, linear 128->1000; batch 64, 3x224x224, "
+               "random weights and inputs")
+
+
+def _deep_cnn():
+    import torch
+    nn = torch.nn
+    torch.manual_seed(0)
+    layers = [nn.Conv2d(3, 128, 3, stride=2, padding=1), nn.ReLU()]
+    for _ in range(12):
+        layers += [nn.Conv2d(128, 128, 3, padding=1), nn.ReLU()]
+    layers += [nn.AdaptiveAvgPool2d(1), nn.Flatten(), nn.Linear(128, 1000)]
+    return nn.Sequential(*layers).cuda()
+
+
+def run_train(args):
+    """The path inside a training step (the vDNN setting of section V.D): forward and
+    backward of a CNN whose saved activations are (a) kept in HBM, (b) compressed and
+    offloaded to pinned host memory during forward and prefetched back during backward, or
+    (c) kept compressed in HBM. Reports time per step, peak device memory and the
+    compression of the saved activations; the gradients of (b) and (c) must equal (a)'s
+    bit for bit."""
+    import torch
+
+    from activation_sparsity_compression_gb300 import build as zbuild
+    zbuild.build()
+    from activation_sparsity_compression_gb300.offload import ActivationOffload
+
+    torch.backends.cudnn.deterministic = True
+    torch.backends.cudnn.benchmark = False
+    model = _deep_cnn()
+    g = torch.Generator(device="cuda").manual_seed(1)
+    x = torch.randn(64, 3, 224, 224, device="cuda", generator=g)
+
+    def step(off):
+        model.zero_grad(set_to_none=True)
+        if off is None:
+            loss = model(x).square().mean()
+        else:
+            with off:
+                loss = model(x).square().mean()
+        loss.backward()
+
+    res, grads = {}, {}
+    steps = max(3, min(args.steps, 20))
+    for mode in ("keep", "host", "device"):
+        off = None if mode == "keep" else ActivationOffload(where=mode)
+        for _ in range(max(args.warmup, 2)):
+            step(off)
+        torch.cuda.synchronize()
+        torch.cuda.reset_peak_memory_stats()
+        base = torch.cuda.memory_allocated()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step(off)
+        e1.record()
+        torch.cuda.synchronize()
+        if off is not None:
+            off.check_errors()
+        grads[mode] = [p.grad.clone() for p in model.parameters()]
+        r = {"ms_per_step": e0.elapsed_time(e1) / steps,
+             "peak_extra_gb": (torch.cuda.max_memory_allocated() - base) / 1e9}
+        if off is not None:
+            st = off.stats
+            passes = max(args.warmup, 2) + steps
+            r["compressed_gb_in_per_step"] = st["bytes_in"] / passes / 1e9
+            r["compressed_gb_out_per_step"] = st["bytes_stored"] / passes / 1e9
+            r["ratio"] = st["bytes_in"] / max(st["bytes_stored"], 1)
+        res[mode] = r
+    identical = all(torch.equal(a, b) for m in ("host", "device")
+                    for a, b in zip(grads["keep"], grads[m]))
+    line = {"metric": "training step with ZVC activation offload", "unit": "ms",
+            "higher_is_better": False, "config": {"model": TRAIN_MODEL},
+            "data": "synthetic", "gradients_bit_identical": identical, "modes": res}
+    print(json.dumps(line), flush=True)
+    return 0 if identical else 1
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.write_traffic:
         return write_traffic(args.write_traffic)
+    if args.train:
+        return run_train(args)
     if args.profile:
         return run_profile_case(args)
     if args.impl == "reference":
