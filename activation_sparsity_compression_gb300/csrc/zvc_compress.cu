@@ -298,15 +298,13 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint3
     if (nwin == kTileWindows && !keep_woff) {
 #pragma unroll
       for (uint32_t j = 0; j < kWinPerWarp; ++j) pos = pack_window(slot, pos, v[j], m[j], lane, lane_below);
-    } else {
-#pragma unroll 1
-      for (uint32_t j = 0; j < kWinPerWarp && w0 + j < nwin; ++j) {
-        if (keep_woff && lane == 0) sm.woff[s][w0 + j] = pos;
-        uint32_t vj = 0, mj = 0;
+    } else {  // chunks start inside tiles (their windows' offsets are kept), or ragged tile
 #pragma unroll
-        for (uint32_t k = 0; k < kWinPerWarp; ++k)
-          if (k == j) { vj = v[k]; mj = m[k]; }
-        pos = pack_window(slot, pos, vj, mj, lane, lane_below);
+      for (uint32_t j = 0; j < kWinPerWarp; ++j) {
+        if (w0 + j < nwin) {
+          if (keep_woff && lane == 0) sm.woff[s][w0 + j] = pos;
+          pos = pack_window(slot, pos, v[j], m[j], lane, lane_below);
+        }
       }
     }
     __syncwarp();

@@ -3,18 +3,21 @@
 // section V.B has the engine expand compressed data into 128-byte lines using the masks'
 // prefix counts as scatter offsets).
 //
-// One warp decodes one chunk, located through the stream's chunk offset table:
+// A chunk, located through the stream's chunk offset table, is decoded by a walker and a
+// scatterer: two warps of a CTA of its own (chunks over 2048 words), or one warp that
+// walks and then scatters (smaller chunks, 8 per CTA). The walker:
 //   validate  batch table (if any), stream header and this chunk's table entries; every
-//             check that fails latches ZVC_ERR_CORRUPT and the warp returns before
-//             touching the chunk, so no access leaves the input or output buffers
-//   stage     the chunk's compressed words are copied into this warp's shared memory by
-//             a 1-D TMA bulk copy (plain loads for the unaligned ends)
+//             check that fails latches ZVC_ERR_CORRUPT before any access to the chunk
+//   stage     the chunk's compressed words are copied into shared memory by a 1-D TMA
+//             bulk copy (plain loads for the unaligned ends), at their 16-byte phase
 //   walk      a window's position depends on every earlier mask, so one lane walks the
-//             masks (position += 1 + popc(mask)), recording each window's offset and mask;
-//             the walk must end exactly at the next chunk's offset
-//   scatter   lane l expands words 4(l mod 8) .. +3 of window 4q + l/8: a set bit at
-//             position b reads packed word popc(mask & (2^b - 1)), a clear bit writes 0;
-//             each step expands sixteen whole 128-byte windows with 16-byte stores
+//             masks (position += 1 + popc(mask)), recording each window's (first value,
+//             mask) and publishing how many windows are recorded every 16 windows; the
+//             walk must end exactly at the next chunk's offset
+// The scatterer expands windows as soon as they are recorded, so with two warps the
+// scatter runs under the walk: lane l expands words 4(l mod 8) .. +3 of window l/8 + 4k of each
+// group of 16 windows, a set bit at position b reading packed word popc(mask & (2^b - 1)),
+// a clear bit writing 0, with 16-byte stores.
 // Extra work items (one per tensor, after the chunks) check the headers of streams that
 // have no chunks; an empty batch gets one item that checks its header and table.
 #include "zvc_internal.cuh"
@@ -22,7 +25,15 @@
 namespace zvc {
 namespace {
 
-constexpr uint32_t kBarrierWords = 16;  // one 8-byte mbarrier per warp, up to 8 warps
+// Shared memory of a CTA: control words, then the chunk buffer (C/32 masks + C words, +3
+// for the 16-byte phase), then the window table (first value, mask) per window.
+struct DecompressCtl {
+  uint64_t full;        // mbarrier of the TMA copy
+  uint32_t progress;    // windows recorded in the table so far
+  uint32_t state;       // 0 running, 1 walked and checked, 2 give up (nothing more to do)
+};
+constexpr uint32_t kCtlWords = 4;       // sizeof(DecompressCtl) / 4
+constexpr uint32_t kPublishEvery = 16;  // the walker publishes its progress every 16 windows
 
 template <int MAXT>
 struct DecompressArgs {
@@ -31,13 +42,15 @@ struct DecompressArgs {
   uint8_t* ws;
   uint64_t total_chunks;
   uint64_t total_items;  // total_chunks + T header checks
+  uint64_t wait_limit_ns;
   uint32_t chunk_elems;
   uint32_t T;
   uint32_t batched;
-  uint32_t warps_per_cta;
   uint32_t buf_words;          // largest valid chunk: C/32 masks + C words
-  uint32_t meta_offset_words;  // per window (position of its first value, mask), 8-byte aligned
-  uint32_t warp_stride_words;  // shared memory per warp: chunk (+3 for its phase), window table
+  uint32_t meta_offset_words;  // window table, 8-byte aligned
+  uint32_t chunks_per_cta;
+  uint32_t solo;               // 1: one warp walks and then scatters its chunk
+  uint32_t slot_words;         // shared memory of one chunk: control, buffer, table
   uint32_t* out[MAXT];
   uint64_t n[MAXT];
   uint64_t chunk_begin[MAXT + 1];
@@ -47,18 +60,24 @@ __device__ __forceinline__ uint64_t get_u64_words(const uint32_t* p) {
   return (uint64_t)p[0] | ((uint64_t)p[1] << 32);
 }
 
-template <int MAXT>
-__global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__ DecompressArgs<MAXT> a) {
-  extern __shared__ __align__(16) uint32_t dsm[];
-  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-  const uint64_t item = (uint64_t)blockIdx.x * a.warps_per_cta + warp;
-  if (item >= a.total_items) return;
-  Control* ctl = reinterpret_cast<Control*>(a.ws);
-  const uint32_t C = a.chunk_elems;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(dsm) + warp;
-  uint32_t* buf = dsm + kBarrierWords + (uint64_t)warp * a.warp_stride_words;
-  uint2* wmeta = reinterpret_cast<uint2*>(buf + a.meta_offset_words);  // (first value, mask)
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
 
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+
+// Warp 0: validate, stage and walk. Returns with ctl.state set to 1 (table complete and
+// checked) or 2 (give up; an error is latched unless the item had no chunk).
+template <int MAXT>
+__device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32_t* dsm,
+                       Control* ec, uint64_t item, uint32_t lane) {
+  const uint32_t C = a.chunk_elems;
+  uint32_t* buf = dsm + kCtlWords;
+  uint2* wmeta = reinterpret_cast<uint2*>(dsm + kCtlWords + a.meta_offset_words);
   const bool is_chunk = item < a.total_chunks;
   uint32_t ti = 0;
   uint64_t c = 0;
@@ -77,6 +96,10 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
   }
   const uint64_t n = ti < a.T ? a.n[ti] : 0;
   const uint64_t nc = ceil_div_u64(n, C);
+  auto give_up = [&](uint32_t code) {
+    if (code != 0 && lane == 0) latch_error(ec, code, item);
+    if (lane == 0) st_release_cta(&ctl.state, 2u);
+  };
 
   // ---- locate and validate the stream (all lanes compute the same values). Every
   // address read here is in bounds by sizes known before the round's loads, so each
@@ -103,13 +126,13 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
     }
   }
   if (ti >= a.T) {  // empty batch: only its header and table exist
-    if (!ok && lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, item);
+    give_up(ok ? 0u : (uint32_t)ZVC_ERR_CORRUPT);
     return;
   }
   const uint64_t table_end = 32 + 8 * nc;
   ok = ok && se - sb >= table_end;
   if (!ok) {
-    if (lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, item);
+    give_up(ZVC_ERR_CORRUPT);
     return;
   }
   const uint32_t* sw = a.in + sb / 4;
@@ -134,7 +157,7 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
          (((start | end) & 3u) == 0) && (end - start) / 4 >= nwin &&
          (end - start) / 4 <= (uint64_t)nwin + count;
   if (!ok || !is_chunk) {
-    if (!ok && lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, item);
+    give_up(ok ? 0u : (uint32_t)ZVC_ERR_CORRUPT);
     return;
   }
 
@@ -148,59 +171,93 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
   const uint32_t head = min(len, (4u - phase) & 3u);
   const uint32_t body = (len - head) & ~3u;
   const uint32_t tail = len - head - body;
-  if (body > 0) {
-    if (lane == 0) {
-      mbar_init(bar, 1);
-      fence_mbar_init();
-      mbar_arrive_expect_tx(bar, body * 4);
-      bulk_g2s(buf + head, cw + head, body * 4, bar);
-    }
+  if (body > 0 && lane == 0) {
+    mbar_arrive_expect_tx(&ctl.full, body * 4);
+    bulk_g2s(buf + head, cw + head, body * 4, &ctl.full);
   }
   if (lane < head) buf[lane] = __ldcs(cw + lane);
   if (lane < tail) buf[head + body + lane] = __ldcs(cw + head + body + lane);
+  __threadfence_block();  // the end words are published with the walker's progress
   __syncwarp();
-  if (body > 0 && !mbar_wait(bar, 0, kDefaultWaitLimitNs)) {
-    if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, item);
+  if (body > 0 && !mbar_wait(&ctl.full, 0, a.wait_limit_ns)) {
+    give_up(ZVC_ERR_TIMEOUT);
     return;
   }
   __syncwarp();
 
   // ---- walk the masks. The chain position -> mask -> next position is the critical
-  // path, so the loop carries nothing else: a window spans at most 33 words, so the k-th
-  // read sits below 33k <= buf_words - 33 and stays in this warp's buffer even for a
-  // corrupt chunk, and since positions only grow, ending exactly at len proves that every
-  // read was inside the chunk.
-  uint32_t good = 1;
+  // path. A window spans at most 33 words, so the k-th read sits below 33k <= buf_words -
+  // 33 and stays in this CTA's buffer even for a corrupt chunk, and since positions only
+  // grow, ending exactly at len proves that every read was inside the chunk. (For a
+  // corrupt chunk the scatterer may already have expanded windows from wrong positions;
+  // the output is then unspecified, but every access stays inside the buffers.)
   if (lane == 0) {
     uint32_t pos = 0, m = 0;
+    for (uint32_t w0 = 0; w0 < nwin; w0 += kPublishEvery) {
+      const uint32_t w1 = min(nwin, w0 + kPublishEvery);
 #pragma unroll 4
-    for (uint32_t w = 0; w < nwin; ++w) {
-      m = buf[pos];
-      wmeta[w] = make_uint2(pos + 1u, m);
-      pos += 1u + __popc(m);
+      for (uint32_t w = w0; w < w1; ++w) {
+        m = buf[pos];
+        wmeta[w] = make_uint2(phase + pos + 1u, m);  // first value, from the buffer's start
+        pos += 1u + __popc(m);
+      }
+      st_release_cta(&ctl.progress, w1);
     }
     const uint32_t ragged = count & (kWindow - 1);
-    good = (pos == len) & (ragged == 0 || (m >> ragged) == 0u);
+    const bool good = (pos == len) & (ragged == 0 || (m >> ragged) == 0u);
+    if (!good) latch_error(ec, ZVC_ERR_CORRUPT, item);
+    st_release_cta(&ctl.state, good ? 1u : 2u);
   }
-  good = __shfl_sync(0xffffffffu, good, 0);
-  if (!good) {
-    if (lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, item);
-    return;
-  }
-  __syncwarp();
+}
 
-  // ---- scatter: lane l expands words e .. e+3 (e = 4(l mod 8)) of windows l/8 + 4k;
-  // four windows per lane are in flight at once
+// Warp 1: expands the recorded windows of its chunk as the walker records them.
+template <int MAXT>
+__device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32_t* dsm,
+                          Control* ec, uint64_t item, uint32_t lane) {
+  if (item >= a.total_chunks) return;  // header checks only: the walker does them
+  const uint32_t C = a.chunk_elems;
+  uint32_t ti = 0;
+  if (MAXT > 1) {
+    uint32_t lo = 0, hi = a.T;
+    while (hi - lo > 1) {
+      const uint32_t mid = (lo + hi) >> 1;
+      if (a.chunk_begin[mid] <= item) lo = mid; else hi = mid;
+    }
+    ti = lo;
+  }
+  const uint64_t c = item - a.chunk_begin[ti];
+  const uint64_t cbeg = c * C;
+  const uint32_t count = (uint32_t)min((uint64_t)C, a.n[ti] - cbeg);
+  const uint32_t nwin = (count + kWindow - 1) / kWindow;
+  const uint32_t* buf = dsm + kCtlWords;
+  const uint2* wmeta = reinterpret_cast<const uint2*>(dsm + kCtlWords + a.meta_offset_words);
   uint32_t* dst = a.out[ti] + cbeg;
   const bool vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
   const uint32_t e = 4u * (lane & 7u);
   const uint32_t below = (1u << e) - 1u;
-  for (uint32_t w0 = lane >> 3; w0 < nwin; w0 += 16) {
+  uint32_t ready = 0;
+  uint64_t t0 = 0;
+  for (uint32_t g0 = 0; g0 < nwin; g0 += kPublishEvery) {
+    const uint32_t need = min(nwin, g0 + kPublishEvery);
+    // wait (bounded) until the walker has recorded this group, or gave up
+    while (ready < need) {
+      ready = ld_acquire_cta(&ctl.progress);
+      if (ready >= need) break;
+      if (ld_acquire_cta(&ctl.state) == 2u) return;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) t0 = now;
+      if (now - t0 > a.wait_limit_ns) {
+        if (lane == 0) latch_error(ec, ZVC_ERR_TIMEOUT, item);
+        return;
+      }
+      __nanosleep(64);
+    }
+    // the group's windows: lane group l/8 takes windows g0 + l/8 + 4k, k = 0..3
     uint4 r[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t w = w0 + 4u * k;
-      const uint2 mo = w < nwin ? wmeta[w] : make_uint2(0u, 0u);
+      const uint32_t w = g0 + (lane >> 3) + 4u * k;
+      const uint2 mo = w < need ? wmeta[w] : make_uint2(0u, 0u);
       const uint32_t m = mo.y;
       uint32_t q = mo.x + __popc(m & below);
       uint32_t v[4];
@@ -214,9 +271,9 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t w = w0 + 4u * k;
+      const uint32_t w = g0 + (lane >> 3) + 4u * k;
+      if (w >= need) break;
       const uint32_t base = w * kWindow + e;
-      if (w >= nwin) break;
       if (vec && base + 4u <= count) {
         *reinterpret_cast<uint4*>(dst + base) = r[k];
       } else {
@@ -229,6 +286,41 @@ __global__ void __launch_bounds__(256) decompress_kernel(const __grid_constant__
   }
 }
 
+// A chunk of up to 2048 words walks in at most 64 steps, so one warp walks it and then
+// expands it, and 8 chunks share a CTA; a larger chunk gets a walker and a scatterer warp
+// and a CTA of its own.
+constexpr uint32_t kSoloChunksPerCta = 8;
+constexpr uint32_t kMaxThreads = 256;
+
+template <int MAXT>
+__global__ void __launch_bounds__(kMaxThreads)
+    decompress_kernel(const __grid_constant__ DecompressArgs<MAXT> a) {
+  extern __shared__ __align__(16) uint32_t dsm_all[];
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t k = a.solo ? warp : warp >> 1;  // this warp's chunk within the CTA
+  uint32_t* dsm = dsm_all + (uint64_t)k * a.slot_words;
+  DecompressCtl& ctl = *reinterpret_cast<DecompressCtl*>(dsm);
+  const uint64_t item = (uint64_t)blockIdx.x * a.chunks_per_cta + k;
+  Control* ec = reinterpret_cast<Control*>(a.ws);
+  if (lane == 0 && (a.solo || (warp & 1u) == 0)) {
+    mbar_init(&ctl.full, 1);
+    fence_mbar_init();
+    ctl.progress = 0;
+    ctl.state = 0;
+  }
+  __syncthreads();
+  if (item >= a.total_items) return;
+  if (a.solo) {
+    walker(a, ctl, dsm, ec, item, lane);
+    __syncwarp();
+    scatterer(a, ctl, dsm, ec, item, lane);
+  } else if ((warp & 1u) == 0) {
+    walker(a, ctl, dsm, ec, item, lane);
+  } else {
+    scatterer(a, ctl, dsm, ec, item, lane);
+  }
+}
+
 template <int MAXT>
 zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, uint32_t T,
                     bool batched, uint32_t C, uint8_t* ws, cudaStream_t stream) {
@@ -236,6 +328,7 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   args.in = in;
   args.in_bytes = in_bytes;
   args.ws = ws;
+  args.wait_limit_ns = kDefaultWaitLimitNs;
   args.chunk_elems = C;
   args.T = T;
   args.batched = batched ? 1u : 0u;
@@ -252,18 +345,17 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   const uint32_t wpc = C / kWindow;
   args.buf_words = wpc + C;
   args.meta_offset_words = (uint32_t)round_up_u64(args.buf_words + 4, 2);
-  args.warp_stride_words = (uint32_t)round_up_u64(args.meta_offset_words + 2ull * wpc, 4);
-  const uint64_t per_warp = 4ull * args.warp_stride_words;
-  uint32_t warps = (uint32_t)(73728ull / per_warp);
-  warps = warps < 1 ? 1 : (warps > 8 ? 8 : warps);
-  args.warps_per_cta = warps;
-  const uint64_t smem = 4ull * kBarrierWords + per_warp * warps;
+  args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.meta_offset_words + 2ull * wpc, 4);
+  args.solo = C <= 2048 ? 1u : 0u;
+  args.chunks_per_cta = args.solo ? kSoloChunksPerCta : 1u;
+  const uint32_t threads = args.solo ? 32u * kSoloChunksPerCta : 64u;
+  const uint64_t smem = 4ull * args.slot_words * args.chunks_per_cta;
   cudaError_t e = cudaFuncSetAttribute(decompress_kernel<MAXT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_failure(e);
-  const uint64_t blocks = ceil_div_u64(args.total_items, warps);
+  const uint64_t blocks = ceil_div_u64(args.total_items, args.chunks_per_cta);
   const TraceMark mark = trace_begin(kTraceDecompress, stream);
-  decompress_kernel<MAXT><<<(unsigned)blocks, 32 * warps, smem, stream>>>(args);
+  decompress_kernel<MAXT><<<(unsigned)blocks, threads, smem, stream>>>(args);
   trace_end(mark, stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_failure(e);
