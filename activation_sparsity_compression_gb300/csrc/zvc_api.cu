@@ -34,7 +34,8 @@ uint64_t stream_floor(uint64_t n, uint32_t c) {
 uint64_t batch_prefix(uint32_t T) { return 16 + 8 * ((uint64_t)T + 1); }
 
 uint64_t compress_ws_bytes(uint64_t total_tiles, uint32_t T) {
-  return round_up_u64(kStatusOffset + 8 * total_tiles + 8 * (uint64_t)T, ZVC_WORKSPACE_ALIGN);
+  return round_up_u64(kStatusOffset + 8 * total_tiles + sizeof(TensorStart) * (uint64_t)T,
+                      ZVC_WORKSPACE_ALIGN);
 }
 
 void put_u32(uint8_t* p, uint32_t v) { std::memcpy(p, &v, 4); }

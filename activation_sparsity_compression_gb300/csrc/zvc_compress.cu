@@ -23,6 +23,9 @@
 //           copy of the slot's next tile
 // The CTA owning the last tile writes the stream header(s), the batch table and the total
 // byte count once that tile knows its place.
+#include <atomic>
+#include <random>
+
 #include "zvc_internal.cuh"
 
 namespace zvc {
@@ -36,6 +39,7 @@ struct CompressArgs {
   uint8_t* ws;
   uint64_t total_tiles;
   uint64_t wait_limit_ns;
+  uint64_t epoch;          // tags this launch's entries in the workspace
   uint64_t hdr_words_end;  // batch prefix + every stream's header and table, in words
   uint32_t chunk_elems;
   uint32_t T;
@@ -48,8 +52,6 @@ struct CompressArgs {
   uint64_t payload_base[MAXT];    // hdr_before + this stream's header and table
 };
 
-using PerCallCounters = Counters;
-static_assert(sizeof(PerCallCounters) <= kCountersBytes, "counter block");
 
 __device__ __forceinline__ void put_u64_words(uint32_t* p, uint64_t v) {
   p[0] = (uint32_t)v;
@@ -149,9 +151,30 @@ __device__ __forceinline__ void fill_slot(const CompressArgs<MAXT>& a, CompressS
 // Headers of every stream and the batch table (one warp). Runs once the last tile knows
 // its place, which gives the total payload; `failed` is set when that tile gave up, in
 // which case a failure upstream has been latched already.
+// A tensor's start in the payload, published by its first tile in this launch (bounded
+// wait); false if that tile gave up or the wait ran out.
+template <int MAXT>
+__device__ bool wait_tensor_start(const CompressArgs<MAXT>& a, const TensorStart* ts, Control* ctl,
+                                  uint64_t info, uint64_t* value) {
+  WaitClock clock;
+  while (true) {
+    const uint64_t tag = ld_acquire_u64(&ts->tag);
+    if ((tag >> 2) == a.epoch) {
+      if ((tag & 3u) == kStartPrefix) {
+        *value = ld_relaxed_u64(&ts->value);
+        return true;
+      }
+      break;
+    }
+    if (!clock.tick(a.wait_limit_ns)) break;
+  }
+  latch_error(ctl, ZVC_ERR_TIMEOUT, info);
+  return false;
+}
+
 template <int MAXT>
 __device__ void finalize_warp(const CompressArgs<MAXT>& a, uint64_t total_payload, bool failed,
-                              const uint64_t* tstart, Control* ctl, uint64_t* pbuf,
+                              const TensorStart* tstart, Control* ctl, uint64_t* pbuf,
                               uint32_t lane) {
   int bad = failed;
   if (lane == 0) {
@@ -164,18 +187,7 @@ __device__ void finalize_warp(const CompressArgs<MAXT>& a, uint64_t total_payloa
       uint64_t p = next;
       if (a.tile_begin[i + 1] > a.tile_begin[i]) {
         p = 0;
-        if (MAXT > 1) {
-          WaitClock clock;
-          while (true) {
-            const uint64_t st = ld_relaxed_u64(tstart + i);
-            if ((st >> kFlagShift) == kFlagPrefix) { p = st & kValueMask; break; }
-            if ((st >> kFlagShift) == kFlagError || !clock.tick(a.wait_limit_ns)) {
-              latch_error(ctl, ZVC_ERR_TIMEOUT, a.total_tiles);
-              bad = 1;
-              break;
-            }
-          }
-        }
+        if (MAXT > 1 && !wait_tensor_start(a, tstart + i, ctl, a.total_tiles, &p)) bad = 1;
       }
       pbuf[i] = p;
       next = p;
@@ -237,7 +249,7 @@ __device__ __forceinline__ uint32_t pack_window(uint32_t* slot, uint32_t pos, ui
 }
 
 template <int MAXT>
-__device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint32_t* aggs,
+__device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint64_t* status,
                           Control* ctl, uint32_t team, uint32_t q, uint32_t lane) {
   const unsigned long long G = gridDim.x;
   const uint32_t lane_below = (1u << lane) - 1u;
@@ -290,7 +302,7 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint3
       agg += x;
     }
     if (q == 0 && lane == 0) {
-      st_relaxed_u32(aggs + t, agg);  // publish the aggregate now
+      st_relaxed_u64(status + t, (a.epoch << kAggBits) | agg);  // publish the aggregate now
       sm.info[s].agg = agg;
     }
     // write back, packed: one store per window, in which the lanes holding a zero write
@@ -319,14 +331,15 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint3
 // sums its window on its own and then adds the previous tile's inclusive prefix, handed
 // over through shared memory.
 template <int MAXT>
-__device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint32_t* aggs,
-                            uint64_t* tstart, Control* ctl, uint32_t k, uint32_t lane) {
+__device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, const uint64_t* status,
+                            TensorStart* tstart, Control* ctl, uint32_t k, uint32_t lane) {
   const unsigned long long G = gridDim.x;
-  uint32_t lb[kLookbackWidth];
+  uint64_t lb[kLookbackWidth];
   uint32_t i = k;
   unsigned long long t = blockIdx.x + k * G;
   if (t < a.total_tiles)
-    aggsum_issue<kLookbackWidth>(aggs, (int64_t)t - 1, i ? (int64_t)(t - G) : -1, lane, lb);
+    aggsum_issue<kLookbackWidth>(status, a.epoch, (int64_t)t - 1, i ? (int64_t)(t - G) : -1,
+                                 lane, lb);
   for (; t < a.total_tiles; i += 2, t += 2 * G) {
     const int s = (int)(i % kSlots);
     if (!mbar_wait(&sm.packed[s], (i / kSlots) & 1u, a.wait_limit_ns)) {
@@ -338,9 +351,11 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
     const uint64_t lt = f.lt;
     const int64_t floor = i ? (int64_t)(t - G) : -1;
     uint64_t excl = 0;
-    bool ok = aggsum_finish<kLookbackWidth>(aggs, t, floor, lane, a.wait_limit_ns, ctl, lb, &excl);
+    bool ok = aggsum_finish<kLookbackWidth>(status, a.epoch, t, floor, lane, a.wait_limit_ns, ctl,
+                                            lb, &excl);
     if (t + 2 * G < a.total_tiles)  // start this warp's next pass
-      aggsum_issue<kLookbackWidth>(aggs, (int64_t)(t + 2 * G) - 1, (int64_t)(t + G), lane, lb);
+      aggsum_issue<kLookbackWidth>(status, a.epoch, (int64_t)(t + 2 * G) - 1, (int64_t)(t + G),
+                                   lane, lb);
     if (i > 0) {  // the CTA's previous tile, from the other settle warp
       const uint32_t h = (i - 1) & 1u;
       if (!mbar_wait(&sm.handoff[h], ((i - 1) / 2) & 1u, a.wait_limit_ns)) {
@@ -365,22 +380,12 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, uin
       uint64_t pstart = 0;
       if (MAXT > 1) {
         if (lt == 0) {
-          st_relaxed_u64(tstart + ti, ok ? ((kFlagPrefix << kFlagShift) | excl)
-                                         : (kFlagError << kFlagShift));
+          st_relaxed_u64(&tstart[ti].value, excl);
+          st_release_u64(&tstart[ti].tag, (a.epoch << 2) | (ok ? kStartPrefix : kStartError));
           pstart = excl;
         } else if (ok) {
           // payload words before this tensor, published by its first tile (a lower tile)
-          WaitClock clock;
-          while (true) {
-            const uint64_t st = ld_relaxed_u64(tstart + ti);
-            const uint64_t fl = st >> kFlagShift;
-            if (fl == kFlagPrefix) { pstart = st & kValueMask; break; }
-            if (fl == kFlagError || !clock.tick(a.wait_limit_ns)) {
-              latch_error(ctl, ZVC_ERR_TIMEOUT, t);
-              ok = false;
-              break;
-            }
-          }
+          ok = wait_tensor_start(a, tstart + ti, ctl, t, &pstart);
         }
       }
       f.dst = dst;
@@ -460,9 +465,9 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
   extern __shared__ __align__(16) uint8_t dsmem[];
   CompressShared& sm = *reinterpret_cast<CompressShared*>(dsmem);
   Control* ctl = reinterpret_cast<Control*>(a.ws);
-  // per tile: its aggregate (u32), in the tile-status area of the workspace
-  uint32_t* aggs = reinterpret_cast<uint32_t*>(a.ws + kStatusOffset);
-  uint64_t* tstart = reinterpret_cast<uint64_t*>(a.ws + kStatusOffset) + a.total_tiles;
+  // per tile: its aggregate, tagged with this launch's epoch; then the tensor starts
+  uint64_t* status = reinterpret_cast<uint64_t*>(a.ws + kStatusOffset);
+  TensorStart* tstart = reinterpret_cast<TensorStart*>(status + a.total_tiles);
   const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
 
   if (a.total_tiles == 0) {  // every tensor empty: headers only
@@ -483,19 +488,35 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
   const unsigned long long G = gridDim.x;
   if (tid == 0)
     for (int s = 0; s < kSlots; ++s) fill_slot(a, sm, s, blockIdx.x + (unsigned long long)s * G);
-  if (warp < kSettleWarp0) pack_role(a, sm, aggs, ctl, warp / kTeamWarps, warp % kTeamWarps, lane);
-  else if (warp < kStoreWarp0) settle_role(a, sm, aggs, tstart, ctl, warp - kSettleWarp0, lane);
+  if (warp < kSettleWarp0) pack_role(a, sm, status, ctl, warp / kTeamWarps, warp % kTeamWarps, lane);
+  else if (warp < kStoreWarp0) settle_role(a, sm, status, tstart, ctl, warp - kSettleWarp0, lane);
   else store_role(a, sm, ctl, warp - kStoreWarp0, lane);
 }
 
-__global__ void lookback_probe_kernel(uint8_t* ws, uint64_t limit_ns) {
+__global__ void lookback_probe_kernel(uint8_t* ws, uint64_t epoch, uint64_t limit_ns) {
   Control* ctl = reinterpret_cast<Control*>(ws);
-  const uint32_t* aggs = reinterpret_cast<const uint32_t*>(ws + kStatusOffset);
-  // tile 1 sums the aggregate of tile 0, which nothing publishes
-  uint32_t v[kLookbackWidth];
+  const uint64_t* status = reinterpret_cast<const uint64_t*>(ws + kStatusOffset);
+  // tile 1 sums the aggregate of tile 0, which nothing publishes in this epoch
+  uint64_t v[kLookbackWidth];
   uint64_t sum = 0;
-  aggsum_issue<kLookbackWidth>(aggs, 0, -1, threadIdx.x & 31u, v);
-  aggsum_finish<kLookbackWidth>(aggs, 1, -1, threadIdx.x & 31u, limit_ns, ctl, v, &sum);
+  aggsum_issue<kLookbackWidth>(status, epoch, 0, -1, threadIdx.x & 31u, v);
+  aggsum_finish<kLookbackWidth>(status, epoch, 1, -1, threadIdx.x & 31u, limit_ns, ctl, v, &sum);
+}
+
+// Epochs of compress launches: a process-wide counter started at a random point below
+// 2^40, so that entries a previous process may have left in reused device memory do not
+// match either, and far below 2^48, so that it never wraps.
+std::atomic<uint64_t> g_epoch{0};
+
+uint64_t next_epoch() {
+  uint64_t e = g_epoch.load();
+  if (e == 0) {
+    std::random_device rd;
+    const uint64_t seed = (((uint64_t)rd() << 32) ^ rd()) & ((1ull << 40) - 1);
+    uint64_t expected = 0;
+    g_epoch.compare_exchange_strong(expected, seed | 1);
+  }
+  return g_epoch.fetch_add(1) + 1;
 }
 
 template <int MAXT>
@@ -508,6 +529,7 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
   args.out_size = out_size;
   args.ws = ws;
   args.wait_limit_ns = limit_ns;
+  args.epoch = next_epoch();
   args.chunk_elems = C;
   args.T = T;
   args.batched = batched ? 1u : 0u;
@@ -543,8 +565,6 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
       return cuda_failure(e);
     resident = sms * (per_sm > 0 ? per_sm : 1);
   }
-  e = cudaMemsetAsync(ws + kPerCallOffset, 0, per_call_bytes(tiles, T), stream);
-  if (e != cudaSuccess) return cuda_failure(e);
   const uint64_t grid = tiles == 0 ? 1 : (tiles < (uint64_t)resident ? tiles : (uint64_t)resident);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -580,10 +600,8 @@ zvc_status launch_compress(const TensorIn* ts, uint32_t T, bool batched, uint32_
 }
 
 zvc_status launch_lookback_timeout_probe(uint8_t* ws, uint64_t limit_ns, cudaStream_t stream) {
-  cudaError_t e = cudaMemsetAsync(ws + kPerCallOffset, 0, per_call_bytes(2, 1), stream);
-  if (e != cudaSuccess) return cuda_failure(e);
-  lookback_probe_kernel<<<1, 32, 0, stream>>>(ws, limit_ns);
-  e = cudaGetLastError();
+  lookback_probe_kernel<<<1, 32, 0, stream>>>(ws, next_epoch(), limit_ns);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_failure(e);
   return ZVC_OK;
 }

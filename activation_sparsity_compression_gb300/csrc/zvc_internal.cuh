@@ -21,35 +21,35 @@ constexpr uint32_t kBatchHeaderWords = 4;       // 16 bytes
 
 // Workspace layout (device memory owned by the caller, 256-byte aligned).
 //   [0, 256)        Control: latched error, persists across calls until zvc_get_error.
-//   [256, 512)      Counters: finished and failed tile counts, cleared by every call.
-//   [512, ...)      u64 tile_status[tiles], then u64 tensor_start[T], cleared by every call.
+//   [256, 512)      reserved.
+//   [512, ...)      u64 tile status[tiles], then TensorStart[T] (compress only).
+// The status entries carry the epoch of the launch that wrote them (a number the host
+// draws anew for every compress launch), so entries left by earlier launches never match
+// and nothing needs clearing between calls.
 struct Control {
   uint32_t error;       // first zvc_status latched on the device, 0 if none
   uint32_t pad;
   uint64_t error_info;  // tile or chunk index of that error
 };
-struct Counters {
-  unsigned long long unused;
-  unsigned long long done;    // tiles that have published their place
-  unsigned long long failed;  // tiles that gave up
-};
 constexpr uint64_t kControlBytes = 256;
-constexpr uint64_t kCountersBytes = 256;
-constexpr uint64_t kPerCallOffset = kControlBytes;  // counters + status arrays start here
-constexpr uint64_t kStatusOffset = kControlBytes + kCountersBytes;
+constexpr uint64_t kStatusOffset = 512;
 
-// Look-back status word: 2-bit flag in bits 63..62, payload word count in bits 61..0.
-constexpr uint64_t kFlagShift = 62;
-constexpr uint64_t kFlagInvalid = 0;    // nothing published yet
-constexpr uint64_t kFlagAggregate = 1;  // value = this tile's own compressed words
-constexpr uint64_t kFlagPrefix = 2;     // value = compressed words of this tile and all before it
-constexpr uint64_t kFlagError = 3;      // this tile gave up; successors give up too
-constexpr uint64_t kValueMask = (1ull << kFlagShift) - 1;
+// Tile status word: the launch's epoch in bits 63..16 and the tile's payload words (an
+// aggregate: at most 4224) in bits 15..0.
+constexpr uint32_t kAggBits = 16;
+constexpr uint64_t kAggMask = (1ull << kAggBits) - 1;
+constexpr uint64_t kEpochLimit = 1ull << (64 - kAggBits);
 
-// Compress tiling: one CTA of 256 threads per tile of 4096 words (128 windows); every
-// thread holds 16 words as four 16-byte vectors.
-constexpr int kCompressThreads = 256;
-constexpr int kCompressWarps = kCompressThreads / 32;
+// A tensor's start in the payload (batched compress), published by the tensor's first
+// tile: `value` first, then `tag` = epoch << 2 | flag with release semantics.
+struct TensorStart {
+  uint64_t value;  // payload words before the tensor
+  uint64_t tag;
+};
+constexpr uint64_t kStartPrefix = 2;  // value is valid
+constexpr uint64_t kStartError = 3;   // the first tile gave up
+
+// Compress tiling: tiles of 4096 words (128 windows).
 constexpr uint32_t kTileElems = 4096;
 constexpr uint32_t kTileWindows = kTileElems / kWindow;
 
@@ -62,11 +62,6 @@ __host__ __device__ inline uint64_t ceil_div_u64(uint64_t a, uint64_t b) {
 inline uint64_t round_up_u64(uint64_t a, uint64_t b) { return ceil_div_u64(a, b) * b; }
 
 inline uint64_t tiles_for(uint64_t n) { return ceil_div_u64(n, kTileElems); }
-
-// Bytes of the per-call region (counters + tile status + tensor starts).
-inline uint64_t per_call_bytes(uint64_t total_tiles, uint32_t T) {
-  return kCountersBytes + 8 * total_tiles + 8 * (uint64_t)T;
-}
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
@@ -87,6 +82,16 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
 
 __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -117,183 +122,31 @@ struct WaitClock {
   }
 };
 
-// Decoupled look-back (Merrill and Garland, "Single-pass Parallel Prefix Scan with
-// Decoupled Look-back", 2016), warp-collective and wide: one pass reads 32*K predecessors. Load j of lane l reads the
-// tile at distance 32j + l + 1, so each load instruction of the warp reads 32 consecutive
-// status words (two cache lines): with every tile of a round looking back over the same
-// few lines at once, uncoalesced reads would queue up on those L2 lines. The nearest
-// inclusive prefix is the smallest distance with a prefix flag; every entry up to it
-// counts. A pass can be issued early (lookback_issue) and evaluated later, so that its
-// L2 round trip overlaps other work.
-template <int K>
-__device__ __forceinline__ void lookback_issue(const uint64_t* status, int64_t top, uint32_t lane,
-                                               uint64_t (&s)[K], int64_t floor = -1,
-                                               uint64_t floor_prefix = 0) {
-  // Entries at or below `floor` are not read: the tile at `floor` acts as an inclusive
-  // prefix of floor_prefix words (the caller's own earlier tile, or "nothing" at -1).
-#pragma unroll
-  for (int j = 0; j < K; ++j) {
-    const int64_t idx = top - 32 * j - (int64_t)lane;
-    s[j] = idx > floor ? ld_relaxed_u64(status + idx)
-                       : ((kFlagPrefix << kFlagShift) | (idx == floor ? floor_prefix : 0));
-  }
-}
-
-enum LookbackPassResult { kPassPrefix = 0, kPassAllAggregates = 1, kPassUnpublished = 2, kPassFailed = 3 };
-
-// Evaluates one pass (warp-collective). On kPassPrefix / kPassAllAggregates, *part is the
-// sum of the counted entries (the whole window for kPassAllAggregates). Aggregates are at
-// most one tile of words each, so the aggregates of one window sum in 32 bits; only the
-// nearest prefix needs 64.
-template <int K>
-__device__ __forceinline__ int lookback_eval(const uint64_t (&s)[K], uint32_t lane, uint64_t* part,
-                                             uint32_t* prefix_dist = nullptr) {
-  uint32_t jl = K;  // this lane's nearest prefix
-#pragma unroll
-  for (int j = K - 1; j >= 0; --j)
-    if ((s[j] >> kFlagShift) == kFlagPrefix) jl = j;
-  const uint32_t jstar = __reduce_min_sync(0xffffffffu, jl);
-  const uint32_t lanes_at = __ballot_sync(0xffffffffu, jl == jstar);
-  const uint32_t lstar = jstar < K ? (uint32_t)(__ffs(lanes_at) - 1) : 31u;
-  bool unpublished = false, failed = false;
-  uint32_t aggs = 0;
-  uint64_t prefix = 0;
-#pragma unroll
-  for (int j = 0; j < K; ++j) {
-    const bool counted = (uint32_t)j < jstar || ((uint32_t)j == jstar && lane <= lstar);
-    if (counted) {
-      const uint64_t f = s[j] >> kFlagShift;
-      unpublished |= (f == kFlagInvalid);
-      failed |= (f == kFlagError);
-      if (f == kFlagPrefix) prefix = s[j] & kValueMask;
-      else aggs += (uint32_t)(s[j] & kValueMask);
-    }
-  }
-  if (__any_sync(0xffffffffu, failed)) return kPassFailed;
-  if (__any_sync(0xffffffffu, unpublished)) return kPassUnpublished;
-  aggs = __reduce_add_sync(0xffffffffu, aggs);
-  if (jstar < K) {
-    prefix = __shfl_sync(0xffffffffu, prefix, lstar);
-    *part = prefix + aggs;
-    if (prefix_dist) *prefix_dist = 32 * jstar + lstar + 1;  // distance below the pass's top + 1
-    return kPassPrefix;
-  }
-  *part = aggs;
-  return kPassAllAggregates;
-}
-
-// Completes the look-back of `tile` (warp-collective) starting from a pass `s` already
-// issued for top = tile - 1 (with the same floor). On success *excl is the number of
-// payload words in all tiles before `tile`. Returns false (and latches an error) if a predecessor failed or the wait
-// ran past limit_ns.
-template <int K>
-__device__ __forceinline__ bool lookback_finish(uint64_t* status, uint64_t tile, uint32_t lane,
-                                                uint64_t limit_ns, Control* ctl, uint64_t (&s)[K],
-                                                uint64_t* excl, int64_t floor = -1,
-                                                uint64_t floor_prefix = 0) {
-  uint64_t sum = 0;
-  int64_t top = (int64_t)tile - 1;
-  WaitClock clock;
-  while (true) {
-    uint64_t part = 0;
-    const int r = lookback_eval<K>(s, lane, &part);
-    if (r == kPassFailed) {
-      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
-      return false;
-    }
-    if (r == kPassUnpublished) {
-      bool alive = true;
-      if (lane == 0) alive = clock.tick(limit_ns);
-      alive = __shfl_sync(0xffffffffu, alive, 0);
-      if (!alive) {
-        if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
-        return false;
-      }
-    } else {
-      sum += part;
-      if (r == kPassPrefix) break;
-      top -= 32 * K;
-    }
-    lookback_issue<K>(status, top, lane, s, floor, floor_prefix);
-  }
-  *excl = sum;
-  return true;
-}
-
-// As lookback_finish, for a look-back bounded below by `floor`, the caller's own earlier
-// tile, whose inclusive prefix may not be known yet: the floor is read as a prefix of 0
-// words and *at_floor tells whether the walk ended there, in which case the caller adds
-// the floor tile's inclusive prefix to *excl.
-template <int K>
-__device__ __forceinline__ bool lookback_to_floor(uint64_t* status, uint64_t tile, uint32_t lane,
-                                                  uint64_t limit_ns, Control* ctl, uint64_t (&s)[K],
-                                                  int64_t floor, uint64_t* excl, bool* at_floor) {
-  uint64_t sum = 0;
-  int64_t top = (int64_t)tile - 1;
-  WaitClock clock;
-  while (true) {
-    uint64_t part = 0;
-    uint32_t dist = 0;
-    const int r = lookback_eval<K>(s, lane, &part, &dist);
-    if (r == kPassFailed) {
-      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
-      return false;
-    }
-    if (r == kPassUnpublished) {
-      bool alive = true;
-      if (lane == 0) alive = clock.tick(limit_ns);
-      alive = __shfl_sync(0xffffffffu, alive, 0);
-      if (!alive) {
-        if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, tile);
-        return false;
-      }
-    } else {
-      sum += part;
-      if (r == kPassPrefix) {
-        *at_floor = (top + 1 - (int64_t)dist) == floor;
-        break;
-      }
-      top -= 32 * K;
-    }
-    lookback_issue<K>(status, top, lane, s, floor, 0);
-  }
-  *excl = sum;
-  return true;
-}
-
-template <int K>
-__device__ __forceinline__ bool lookback_exclusive_wide(uint64_t* status, uint64_t tile,
-                                                        uint32_t lane, uint64_t limit_ns,
-                                                        Control* ctl, uint64_t* excl) {
-  uint64_t s[K];
-  lookback_issue<K>(status, (int64_t)tile - 1, lane, s);
-  return lookback_finish<K>(status, tile, lane, limit_ns, ctl, s, excl);
-}
-
-// Bounded look-back over tile aggregates. Each tile publishes its aggregate (its payload
-// words, at least 1, so 0 means "not yet") in aggs[tile]. A tile whose caller already
-// knows the inclusive prefix of an earlier tile `floor` needs only the sum of the
+// Bounded look-back over tile aggregates (after Merrill and Garland, "Single-pass
+// Parallel Prefix Scan with Decoupled Look-back", 2016). Each tile publishes its aggregate
+// (its payload words) in status[tile], tagged with the launch's epoch. A tile whose caller
+// already knows the inclusive prefix of an earlier tile `floor` needs only the sum of the
 // aggregates strictly between floor and itself. One pass reads 32*K of them: load j of
 // lane l reads the tile at distance 32j + l + 1 below `top + 1`, so every warp load
 // instruction reads 32 consecutive words. A window of at most one tile's words per entry
 // sums in 32 bits (32*K * 4224 < 2^32 for K <= 31).
 template <int K>
-__device__ __forceinline__ void aggsum_issue(const uint32_t* aggs, int64_t top, int64_t floor,
-                                             uint32_t lane, uint32_t (&v)[K]) {
+__device__ __forceinline__ void aggsum_issue(const uint64_t* status, uint64_t epoch, int64_t top,
+                                             int64_t floor, uint32_t lane, uint64_t (&v)[K]) {
 #pragma unroll
   for (int j = 0; j < K; ++j) {
     const int64_t idx = top - 32 * j - (int64_t)lane;
-    v[j] = idx > floor ? ld_relaxed_u32(aggs + idx) : 1u;  // below the floor: a placeholder
+    v[j] = idx > floor ? ld_relaxed_u64(status + idx) : (epoch << kAggBits);  // a placeholder
   }
 }
 
-// Sum of aggs(floor, tile) (warp-collective), starting from a pass `v` already issued with
-// top = tile - 1. Returns false (and latches ZVC_ERR_TIMEOUT) if an aggregate is still
-// missing after limit_ns.
+// Sum of the aggregates in (floor, tile) (warp-collective), starting from a pass `v`
+// already issued with top = tile - 1. Returns false (and latches ZVC_ERR_TIMEOUT) if an
+// aggregate is still missing after limit_ns.
 template <int K>
-__device__ __forceinline__ bool aggsum_finish(const uint32_t* aggs, uint64_t tile, int64_t floor,
-                                              uint32_t lane, uint64_t limit_ns, Control* ctl,
-                                              uint32_t (&v)[K], uint64_t* sum_out) {
+__device__ __forceinline__ bool aggsum_finish(const uint64_t* status, uint64_t epoch, uint64_t tile,
+                                              int64_t floor, uint32_t lane, uint64_t limit_ns,
+                                              Control* ctl, uint64_t (&v)[K], uint64_t* sum_out) {
   uint64_t sum = 0;
   int64_t top = (int64_t)tile - 1;
   WaitClock clock;
@@ -303,8 +156,8 @@ __device__ __forceinline__ bool aggsum_finish(const uint32_t* aggs, uint64_t til
 #pragma unroll
     for (int j = 0; j < K; ++j) {
       if (top - 32 * j - (int64_t)lane > floor) {
-        missing |= (v[j] == 0u);
-        part += v[j];
+        missing |= (v[j] >> kAggBits) != epoch;
+        part += (uint32_t)(v[j] & kAggMask);
       }
     }
     if (__any_sync(0xffffffffu, missing)) {
@@ -320,7 +173,7 @@ __device__ __forceinline__ bool aggsum_finish(const uint32_t* aggs, uint64_t til
       top -= 32 * K;
       if (top <= floor) break;
     }
-    aggsum_issue<K>(aggs, top, floor, lane, v);
+    aggsum_issue<K>(status, epoch, top, floor, lane, v);
   }
   *sum_out = sum;
   return true;
@@ -429,8 +282,9 @@ zvc_status launch_decompress(const uint32_t* in, uint64_t in_bytes, const Tensor
                              uint32_t T, bool batched, uint32_t chunk_elems, uint8_t* ws,
                              cudaStream_t stream);
 
-// Runs the look-back on a tile whose predecessor never publishes, with the given limit;
-// the wait must give up and latch ZVC_ERR_TIMEOUT. Used by the self-test entry point.
+// Runs the look-back on a tile whose predecessor never publishes (in this launch's
+// epoch), with the given limit; the wait must give up and latch ZVC_ERR_TIMEOUT. Used by
+// the self-test entry point.
 zvc_status launch_lookback_timeout_probe(uint8_t* ws, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace zvc

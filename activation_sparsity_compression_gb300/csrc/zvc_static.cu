@@ -20,10 +20,11 @@
 
 namespace {
 
-// Control block + counters + one status word per 4096-word tile for up to
-// ZVC_STATIC_MAX_ELEMS words, rounded up to a whole 4 KiB page.
+// Control block, reserved block, one status word per 4096-word tile for up to
+// ZVC_STATIC_MAX_ELEMS words and one tensor start, rounded up to a whole 4 KiB page.
 constexpr uint64_t kStaticScratchBytes = 1052672;  // 1 MiB + 4 KiB
-static_assert(zvc::kStatusOffset + 8 * (ZVC_STATIC_MAX_ELEMS / zvc::kTileElems) + 8 <=
+static_assert(zvc::kStatusOffset + 8 * (ZVC_STATIC_MAX_ELEMS / zvc::kTileElems) +
+                      sizeof(zvc::TensorStart) <=
                   kStaticScratchBytes,
               "static scratch too small for ZVC_STATIC_MAX_ELEMS");
 

@@ -76,8 +76,10 @@ uint64_t zvc_size_bound(uint64_t n, uint32_t chunk_elems);
  * ns is a host array of T word counts. Returns 0 on invalid arguments. */
 uint64_t zvc_batch_size_bound(const uint64_t* ns, uint32_t T, uint32_t chunk_elems);
 
-/* Workspace bytes for zvc_compress / zvc_decompress of n words (look-back tile status,
- * counters and the latched error word). */
+/* Workspace bytes for zvc_compress / zvc_decompress of n words: the latched error word,
+ * then one look-back status word per 4096-word tile. Each compress launch tags the status
+ * words it writes with a number of its own, so a workspace needs no clearing between
+ * calls; only its error word must start at zero (see the conventions above). */
 uint64_t zvc_workspace_size(uint64_t n, uint32_t chunk_elems);
 
 /* Workspace bytes for the batched calls over the T tensors in ns (host array). */
