@@ -155,3 +155,74 @@ def decode_batch(stream, ns, chunk_elems: int = 4096, lib=None):
     r = lib.zvco_decode_batch(_ptr(s, ctypes.c_uint8), s.size, T, _ptr(ns_a, ctypes.c_uint64),
                               chunk_elems, ptrs)
     return int(r), [y[:int(n)] for y, n in zip(ys, ns_a)]
+
+
+# ------------------------------------------------------------------ RLE (comparison codec)
+# Run-length encoding as the pages' layout-dependent comparison codec (section V.A and
+# VII.A); the layout is documented at the top of ``rle_oracle.c``. A separate library, so
+# that the ZVC oracle above stays exactly as pinned.
+_RLE_SRC = os.path.join(_HERE, "rle_oracle.c")
+_RLE_LIB_PATH = os.path.join(_BUILD_DIR, "librle_oracle.so")
+_rle_lib = None
+
+
+def build_all() -> None:
+    """Compile both oracle libraries (ZVC and RLE)."""
+    build()
+    build(_RLE_SRC, _RLE_LIB_PATH)
+
+
+def rle_load(path: str | None = None):
+    """Load (building first if needed) the RLE oracle library."""
+    global _rle_lib
+
+    def declare(lib):
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        lib.rleo_size_bound.restype = ctypes.c_uint64
+        lib.rleo_size_bound.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        lib.rleo_encode.restype = ctypes.c_int64
+        lib.rleo_encode.argtypes = [u32p, ctypes.c_uint64, ctypes.c_uint32, u8p, ctypes.c_uint64]
+        lib.rleo_decode.restype = ctypes.c_int
+        lib.rleo_decode.argtypes = [u8p, ctypes.c_uint64, u32p, ctypes.c_uint64, ctypes.c_uint32]
+        return lib
+
+    if path is not None:
+        return declare(ctypes.CDLL(path))
+    with _lock:
+        if _rle_lib is None:
+            stale = (not os.path.exists(_RLE_LIB_PATH)
+                     or os.path.getmtime(_RLE_LIB_PATH) < os.path.getmtime(_RLE_SRC))
+            if stale:
+                build(_RLE_SRC, _RLE_LIB_PATH)
+            _rle_lib = declare(ctypes.CDLL(_RLE_LIB_PATH))
+    return _rle_lib
+
+
+def rle_size_bound(n: int, window: int, lib=None) -> int:
+    lib = lib or rle_load()
+    return int(lib.rleo_size_bound(n, window))
+
+
+def rle_encode(x, window: int = 1024, lib=None) -> np.ndarray:
+    """RLE-encode a 4-byte-per-element array (any shape) into one stream (uint8)."""
+    lib = lib or rle_load()
+    w = _u32_words(x)
+    n = w.size
+    cap = int(lib.rleo_size_bound(n, window))
+    if cap == 0:
+        raise OracleError(ERR_INVALID_ARG)
+    out = np.empty(cap, dtype=np.uint8)
+    r = lib.rleo_encode(_ptr(w, ctypes.c_uint32), n, window, _ptr(out, ctypes.c_uint8), cap)
+    if r < 0:
+        raise OracleError(int(r))
+    return out[:r].copy()
+
+
+def rle_decode(stream, n: int, window: int = 1024, lib=None):
+    """Decode one RLE stream. Returns (status, words) with words a uint32 array of n."""
+    lib = lib or rle_load()
+    s = np.ascontiguousarray(stream, dtype=np.uint8).reshape(-1)
+    y = np.full(max(n, 1), _POISON, dtype=np.uint32)
+    r = lib.rleo_decode(_ptr(s, ctypes.c_uint8), s.size, _ptr(y, ctypes.c_uint32), n, window)
+    return int(r), y[:n]

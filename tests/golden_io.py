@@ -15,8 +15,8 @@ def _parse_words(spec: str, n: int) -> np.ndarray:
     return w
 
 
-def load(name: str) -> dict:
-    path = os.path.join(GOLDEN_DIR, name)
+def load(name: str, directory: str = GOLDEN_DIR) -> dict:
+    path = os.path.join(directory, name)
     keys = {}
     hex_bytes = []
     in_expected = False
@@ -39,6 +39,10 @@ def load(name: str) -> dict:
             else:
                 keys[k] = v
     expected = bytes(int(b, 16) for b in hex_bytes)
+    if "window" in keys:  # an RLE vector
+        n = int(keys["n"])
+        return {"name": name, "n": n, "window": int(keys["window"]),
+                "input": _parse_words(keys.get("input", ""), n), "expected": expected}
     c = int(keys["chunk_elems"])
     if "batch" in keys:
         ns = [int(s) for s in keys["batch"].split(",")]
@@ -57,3 +61,14 @@ def all_single():
 
 def all_batch():
     return sorted(f for f in os.listdir(GOLDEN_DIR) if f.endswith(".txt") and load(f)["batch"])
+
+
+RLE_DIR = os.path.join(GOLDEN_DIR, "rle")
+
+
+def all_rle():
+    return sorted(f for f in os.listdir(RLE_DIR) if f.endswith(".txt"))
+
+
+def load_rle(name: str) -> dict:
+    return load(name, RLE_DIR)
