@@ -30,6 +30,7 @@ ZVC_MAX_CHUNK_ELEMS = 32768
 ZVC_MAX_BATCH = 512
 ZVC_WORKSPACE_ALIGN = 256
 ZVC_STATIC_MAX_ELEMS = 1 << 29
+ZVC_RLE_MAX_WINDOW = 4096
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libzvc_gb300.so")
@@ -58,6 +59,10 @@ _SIGS = {
     "zvc_offload_host_bound": (_u64, [_u64, _u32]),
     "zvc_offload_workspace_size": (_u64, [_u64, _u32]),
     "zvc_compress_static_get_error": (_st, [_vp]),
+    "zvc_rle_size_bound": (_u64, [_u64, _u32]),
+    "zvc_rle_workspace_size": (_u64, [_u64, _u32]),
+    "zvc_rle_compress": (_st, [_vp, _u64, _u32, _vp, _u64, _vp, _vp, _u64, _vp]),
+    "zvc_rle_decompress": (_st, [_vp, _u64, _vp, _u64, _u32, _vp, _u64, _vp]),
     "zvc_offload_join": (_st, [_vp]),
     "zvc_offload": (_st, [_vp, _u64, _u32, _vp, _u64, ctypes.POINTER(_u64), _vp, _u64, _vp]),
     "zvc_prefetch": (_st, [_vp, _u64, _vp, _u64, _u32, _vp, _u64, _vp]),
@@ -181,6 +186,23 @@ def zvc_offload(d_in, n, chunk_elems, h_pinned, h_cap, d_ws, ws_bytes, stream):
     st = int(lib().zvc_offload(d_in, n, chunk_elems, h_pinned, h_cap, ctypes.byref(size), d_ws,
                                ws_bytes, stream))
     return st, int(size.value)
+
+
+def zvc_rle_size_bound(n, window):
+    return int(lib().zvc_rle_size_bound(n, window))
+
+
+def zvc_rle_workspace_size(n, window):
+    return int(lib().zvc_rle_workspace_size(n, window))
+
+
+def zvc_rle_compress(d_in, n, window, d_out, out_cap, d_out_size, d_ws, ws_bytes, stream):
+    return int(lib().zvc_rle_compress(d_in, n, window, d_out, out_cap, d_out_size, d_ws, ws_bytes,
+                                      stream))
+
+
+def zvc_rle_decompress(d_in, in_bytes, d_out, n, window, d_ws, ws_bytes, stream):
+    return int(lib().zvc_rle_decompress(d_in, in_bytes, d_out, n, window, d_ws, ws_bytes, stream))
 
 
 def zvc_offload_join(stream):

@@ -505,6 +505,50 @@ zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint
   return ZVC_OK;
 }
 
+// ---------------------------------------------------------------- RLE comparison codec
+bool rle_window_ok(uint32_t w) { return w >= 32 && w % 32 == 0 && w <= ZVC_RLE_MAX_WINDOW; }
+
+uint64_t zvc_rle_size_bound(uint64_t n, uint32_t window) {
+  if (!rle_window_ok(window) || n > kMaxElems) return 0;
+  return 32 + 12 * ceil_div_u64(n, window) + 4 * n;
+}
+
+uint64_t zvc_rle_workspace_size(uint64_t n, uint32_t window) {
+  if (!rle_window_ok(window) || n > kMaxElems) return 0;
+  return rle_ws_bytes(n, window);
+}
+
+zvc_status zvc_rle_compress(const void* d_in, uint64_t n, uint32_t window, void* d_out,
+                            uint64_t out_cap, uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
+                            void* stream) {
+  if (!rle_window_ok(window) || n > kMaxElems || d_out == nullptr || d_ws == nullptr ||
+      (n > 0 && d_in == nullptr) || !aligned(d_in, 4) || !aligned(d_out, 8) ||
+      !aligned(d_out_size, 8) || !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
+    return ZVC_ERR_INVALID_ARG;
+  if (out_cap < zvc_rle_size_bound(n, window) || ws_bytes < rle_ws_bytes(n, window))
+    return ZVC_ERR_BUFFER_TOO_SMALL;
+  return launch_rle_compress(static_cast<const uint32_t*>(d_in), n, window,
+                             static_cast<uint32_t*>(d_out), d_out_size,
+                             static_cast<uint8_t*>(d_ws), static_cast<cudaStream_t>(stream));
+}
+
+zvc_status zvc_rle_decompress(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,
+                              uint32_t window, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!rle_window_ok(window) || n > kMaxElems || d_in == nullptr || d_ws == nullptr ||
+      (n > 0 && d_out == nullptr) || !aligned(d_in, 8) || !aligned(d_out, 4) ||
+      !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
+    return ZVC_ERR_INVALID_ARG;
+  if (ws_bytes < kControlBytes) return ZVC_ERR_BUFFER_TOO_SMALL;
+  const uint64_t nwin = ceil_div_u64(n, window);
+  // sizes no valid stream of n words can have: at least one record per window, at most
+  // the bound
+  if (in_bytes % 4 != 0 || in_bytes < 32 + 12 * nwin || in_bytes > zvc_rle_size_bound(n, window))
+    return ZVC_ERR_CORRUPT;
+  return launch_rle_decompress(static_cast<const uint32_t*>(d_in), in_bytes,
+                               static_cast<uint32_t*>(d_out), n, window,
+                               static_cast<uint8_t*>(d_ws), static_cast<cudaStream_t>(stream));
+}
+
 zvc_status zvc_get_error(void* d_ws, void* stream) {
   if (d_ws == nullptr || !aligned(d_ws, ZVC_WORKSPACE_ALIGN)) return ZVC_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -282,6 +282,13 @@ zvc_status launch_decompress(const uint32_t* in, uint64_t in_bytes, const Tensor
                              uint32_t T, bool batched, uint32_t chunk_elems, uint8_t* ws,
                              cudaStream_t stream);
 
+// RLE comparison codec (window of W words, 32 <= W <= ZVC_RLE_MAX_WINDOW).
+uint64_t rle_ws_bytes(uint64_t n, uint32_t W);
+zvc_status launch_rle_compress(const uint32_t* in, uint64_t n, uint32_t W, uint32_t* out,
+                               uint64_t* out_size, uint8_t* ws, cudaStream_t stream);
+zvc_status launch_rle_decompress(const uint32_t* in, uint64_t in_bytes, uint32_t* y, uint64_t n,
+                                 uint32_t W, uint8_t* ws, cudaStream_t stream);
+
 // Runs the look-back on a tile whose predecessor never publishes (in this launch's
 // epoch), with the given limit; the wait must give up and latch ZVC_ERR_TIMEOUT. Used by
 // the self-test entry point.

@@ -214,6 +214,41 @@ zvc_status zvc_trace_stop(uint64_t* launches, double* device_ms);
  * last call (ZVC_OK if none) and clears it. */
 zvc_status zvc_get_error(void* d_ws, void* stream);
 
+/* ---------------------------------------------------------------------------------
+ * Run-length encoding: the layout-dependent comparison codec of section V.A (RLE
+ * exploits runs of zeros and of non-zeros, so its ratio depends on how the values are
+ * laid out) and section VII.A (per 4 KB window; ZVC's ratio does not depend on the
+ * layout, RLE's does). Not on the offload path: it is here to measure that comparison.
+ *
+ * RLE stream (little-endian, this project's reading: the pages give no byte layout):
+ * u32 magic 0x31454C52 ("RLE1"), u16 version 1, u16 word_bytes 4, u32 window W, u32 0,
+ * u64 n, u64 payload_bytes; u64 window_off[ceil(n/W)] (byte offset of each window's
+ * records from the payload start); then per window of W words (the last may be shorter)
+ * records of u16 zeros, u16 literals and `literals` words, where a record is the maximal
+ * zero run at the cursor followed by the maximal non-zero run after it.
+ * Size: 32 + 8 nw + 4 (records + non-zeros), at most 32 + 12 nw + 4 n. */
+#define ZVC_RLE_MAX_WINDOW 4096u    /* words; the paper's 4 KB window is 1024 */
+
+/* Worst-case RLE stream bytes for n words in windows of W (0 on invalid arguments). */
+uint64_t zvc_rle_size_bound(uint64_t n, uint32_t window);
+
+/* Workspace bytes for zvc_rle_compress (window sizes and scan totals). */
+uint64_t zvc_rle_workspace_size(uint64_t n, uint32_t window);
+
+/* RLE-compress n words at d_in (4-byte aligned) into d_out (8-byte aligned, out_cap >=
+ * zvc_rle_size_bound), writing the stream's byte count to *d_out_size (device, 8-byte
+ * aligned). Reads the input twice (window sizes, then the records); asynchronous. */
+zvc_status zvc_rle_compress(const void* d_in, uint64_t n, uint32_t window, void* d_out,
+                            uint64_t out_cap, uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
+                            void* stream);
+
+/* Decompress the RLE stream of in_bytes bytes at d_in (8-byte aligned) into n words at
+ * d_out. Host-visible size errors return ZVC_ERR_CORRUPT; every other check (header,
+ * window offsets, records covering each window exactly) latches ZVC_ERR_CORRUPT in d_ws
+ * (at least 256 bytes; read it with zvc_get_error), with no access outside the buffers. */
+zvc_status zvc_rle_decompress(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,
+                              uint32_t window, void* d_ws, uint64_t ws_bytes, void* stream);
+
 /* The cudaError_t value behind the most recent ZVC_ERR_CUDA on this thread. */
 int zvc_last_cuda_error(void);
 

@@ -24,7 +24,7 @@
  *   offset 16  u64 n
  *   offset 24  u64 payload_bytes
  *   offset 32  u64 window_off[ceil(n / W)]: byte offset of each window's first record,
- *              from the start of the payload
+ *              from the start of the payload (a multiple of 4: records are whole words)
  *   then the payload: the windows' records in order.
  * Size: 32 + 8 * nw + 4 * (records) + 4 * nnz, where a window has one record plus one per
  * zero that follows a non-zero inside it. At most 32 + 12 * nw + 4 * n.
@@ -126,7 +126,8 @@ int rleo_decode(const uint8_t *in, uint64_t in_bytes, uint32_t *y, uint64_t n, u
   for (uint64_t w = 0; w < nw; ++w) {
     const uint64_t off = get_u64(in + 32 + 8 * w);
     const uint64_t next = w + 1 < nw ? get_u64(in + 32 + 8 * (w + 1)) : payload;
-    if ((w == 0 && off != 0) || off > next || next > payload) return RLE_ERR_CORRUPT;
+    if ((w == 0 && off != 0) || off > next || next > payload || (off | next) % 4 != 0)
+      return RLE_ERR_CORRUPT;
     const uint64_t begin = w * window;
     const uint64_t end = begin + window < n ? begin + window : n;
     uint64_t i = begin, pos = payload_at + off;

@@ -54,7 +54,7 @@ def brute_decode(stream, n, window):
     out = []
     for w in range(nw):
         a, b = offs[w], offs[w + 1]
-        if (w == 0 and a != 0) or a > b or b > payload:
+        if (w == 0 and a != 0) or a > b or b > payload or (a | b) % 4:
             return None
         length = min(window, n - w * window)
         got, pos = [], base + a
