@@ -55,6 +55,10 @@ def parse_args(argv=None):
                    help="training step of a VGG-style CNN with its saved activations kept, "
                         "offloaded compressed to host memory, or kept compressed in HBM; "
                         "prints one JSON line and exits")
+    p.add_argument("--layouts", action="store_true",
+                   help="ZVC and RLE compression ratios of the AlexNet stack and the VGG "
+                        "conv1_2 map in NCHW, NHWC and CHWN, and RLE kernel times; prints "
+                        "one JSON line and exits")
     p.add_argument("--write-traffic", nargs=2, metavar=("COMPRESS_CSV", "DECOMPRESS_CSV"),
                    help="turn ncu DRAM counters of one step's launches (see TRAFFIC_FILE) "
                         "into that file, keyed by the kernels' source hashes, and exit")
@@ -697,12 +701,117 @@ def run_train(args):
     return 0 if identical else 1
 
 
+# ------------------------------------------------------------------ layouts: ZVC against RLE
+def run_layouts(args):
+    """Compression ratio (4n / stream bytes) of ZVC and of RLE for the same activations in
+    three layouts (Rhu et al., section VII.A: ZVC's ratio does not depend on the layout,
+    RLE's does), computed by this library's kernels, plus back-to-back kernel times of RLE
+    next to ZVC on AlexNet layer 0."""
+    import torch
+
+    from activation_sparsity_compression_gb300 import build as zbuild
+    zbuild.build()
+    import activation_sparsity_compression_gb300 as zvc
+    import workloads
+
+    C, W = args.chunk_elems, 1024
+    dev = torch.device("cuda", 0)
+    sh = torch.cuda.current_stream(dev).cuda_stream
+
+    def sizes(x):
+        n = x.numel()
+        out = torch.empty(max(zvc.zvc_size_bound(n, C), zvc.zvc_rle_size_bound(n, W)),
+                          dtype=torch.uint8, device=dev)
+        size = torch.zeros(2, dtype=torch.int64, device=dev)
+        ws = zvc.new_workspace(max(zvc.zvc_workspace_size(n, C), zvc.zvc_rle_workspace_size(n, W)),
+                               dev)
+        assert zvc.zvc_compress(x.data_ptr(), n, C, out.data_ptr(), out.numel(), size.data_ptr(),
+                                ws.data_ptr(), ws.numel(), sh) == zvc.ZVC_OK
+        assert zvc.zvc_rle_compress(x.data_ptr(), n, W, out.data_ptr(), out.numel(),
+                                    size.data_ptr() + 8, ws.data_ptr(), ws.numel(), sh) == zvc.ZVC_OK
+        assert zvc.zvc_get_error(ws.data_ptr(), sh) == zvc.ZVC_OK
+        s_zvc, s_rle = (int(v) for v in size.tolist())
+        return 4 * n / s_zvc, 4 * n / s_rle
+
+    layouts = {"NCHW": lambda t: t, "NHWC": lambda t: t.permute(0, 2, 3, 1),
+               "CHWN": lambda t: t.permute(1, 2, 3, 0)}
+    res = {}
+    cases = [("alexnet_stack", workloads.alexnet_stack(device=dev)),
+             ("vgg_conv12", workloads.vgg_conv12(device=dev))]
+    for name, xs in cases:
+        res[name] = {}
+        for lname, f in layouts.items():
+            tot_in = tot_zvc = tot_rle = 0.0
+            for x in xs:
+                t = f(x).contiguous()
+                rz, rr = sizes(t)
+                tot_in += 4 * t.numel()
+                tot_zvc += 4 * t.numel() / rz
+                tot_rle += 4 * t.numel() / rr
+                del t
+            res[name][lname] = {"zvc_ratio": tot_in / tot_zvc, "rle_ratio": tot_in / tot_rle}
+        del xs
+        torch.cuda.empty_cache()
+
+    # kernel times on AlexNet layer 0 (back-to-back launches, CUDA events)
+    x = workloads.alexnet_stack(device=dev)[0]
+    n = x.numel()
+    times = {}
+    for codec in ("zvc", "rle"):
+        cap = zvc.zvc_size_bound(n, C) if codec == "zvc" else zvc.zvc_rle_size_bound(n, W)
+        out = torch.empty(cap, dtype=torch.uint8, device=dev)
+        size = torch.zeros(1, dtype=torch.int64, device=dev)
+        wsb = zvc.zvc_workspace_size(n, C) if codec == "zvc" else zvc.zvc_rle_workspace_size(n, W)
+        ws = zvc.new_workspace(wsb, dev)
+        y = torch.empty_like(x)
+
+        def comp():
+            if codec == "zvc":
+                return zvc.zvc_compress(x.data_ptr(), n, C, out.data_ptr(), cap, size.data_ptr(),
+                                        ws.data_ptr(), ws.numel(), sh)
+            return zvc.zvc_rle_compress(x.data_ptr(), n, W, out.data_ptr(), cap, size.data_ptr(),
+                                        ws.data_ptr(), ws.numel(), sh)
+        assert comp() == zvc.ZVC_OK
+        S = int(size.item())
+
+        def decomp():
+            if codec == "zvc":
+                return zvc.zvc_decompress(out.data_ptr(), S, y.data_ptr(), n, C, ws.data_ptr(),
+                                          ws.numel(), sh)
+            return zvc.zvc_rle_decompress(out.data_ptr(), S, y.data_ptr(), n, W, ws.data_ptr(),
+                                          ws.numel(), sh)
+        r = {}
+        for nm, fn in (("compress", comp), ("decompress", decomp)):
+            fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(10):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / 10
+            r[nm] = {"ms": ms, "gbs_uncompressed": 4 * n / (ms / 1e3) / 1e9}
+        assert zvc.zvc_get_error(ws.data_ptr(), sh) == zvc.ZVC_OK
+        assert torch.equal(y.view(torch.int32), x.view(torch.int32))
+        r["ratio"] = 4 * n / S
+        times[codec] = r
+    line = {"metric": "compression ratio by layout, ZVC vs RLE (4 KB RLE windows)",
+            "unit": "x", "higher_is_better": True, "data": "synthetic",
+            "config": {"zvc_chunk_elems": C, "rle_window": W,
+                       "workloads": ["alexnet_stack batch 128", "vgg_conv12 batch 64"]},
+            "ratios": res, "alexnet_layer0_kernels": times}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.write_traffic:
         return write_traffic(args.write_traffic)
     if args.train:
         return run_train(args)
+    if args.layouts:
+        return run_layouts(args)
     if args.profile:
         return run_profile_case(args)
     if args.impl == "reference":
