@@ -58,12 +58,12 @@ struct SegPlan {
 };
 
 uint64_t segment_elems(uint64_t n, uint32_t c) {
-  // Equal segments of at most about 16 Mi words (64 MiB of fp32), whole chunks. Within a
+  // Equal segments of at most about 32 Mi words (128 MiB of fp32), whole chunks. Within a
   // tensor the copy of one segment overlaps the compression of the next; across tensors
   // the copies of one overlap the compression of the next, so only the first segment's
   // compression and the last one's decompression are exposed, and both kernels run on
   // tens of MB per launch.
-  constexpr uint64_t kTarget = 1ull << 24;
+  constexpr uint64_t kTarget = 1ull << 25;
   const uint64_t count = n == 0 ? 1 : ceil_div_u64(n, kTarget);
   return round_up_u64(ceil_div_u64(n == 0 ? 1 : n, count), c);
 }

@@ -137,8 +137,8 @@ zvc_status zvc_decompress_batched(const void* d_in, uint64_t in_bytes, void* con
                                   void* d_ws, uint64_t ws_bytes, void* stream);
 
 /* Segment length (words) that zvc_offload uses for a tensor of n words: n cut into
- * ceil(n / 2^24) equal parts, rounded up to whole chunks (at most about 16 Mi words,
- * 64 MiB of fp32). */
+ * ceil(n / 2^25) equal parts, rounded up to whole chunks (at most about 32 Mi words,
+ * 128 MiB of fp32). */
 uint64_t zvc_offload_segment_elems(uint64_t n, uint32_t chunk_elems);
 
 /* Host bytes zvc_offload may need: the batch bound over its segments. */

@@ -61,9 +61,9 @@ def test_offload_plan_is_whole_chunks(lib):
     for n in (1, 4096, 8_306_688, 37_171_200, 205_520_896, 2**28):
         seg = zvc.zvc_offload_segment_elems(n, 4096)
         S = -(-n // seg)
-        # ceil(n / 2^24) equal segments of whole chunks, the last one possibly shorter
-        assert seg % 4096 == 0 and seg <= 1 << 24
-        assert S == max(1, -(-n // (1 << 24))) and (S - 1) * seg < n <= S * seg
+        # ceil(n / 2^25) equal segments of whole chunks, the last one possibly shorter
+        assert seg % 4096 == 0 and seg <= 1 << 25
+        assert S == max(1, -(-n // (1 << 25))) and (S - 1) * seg < n <= S * seg
         bound = 16 + 8 * (S + 1) + sum(
             zvc.zvc_size_bound(min(seg, n - k * seg), 4096) for k in range(S))
         assert zvc.zvc_offload_host_bound(n, 4096) == bound
