@@ -76,6 +76,7 @@ constexpr int kSettleWarps = 2;
 constexpr int kStoreWarp0 = kSettleWarp0 + kSettleWarps;     // warps 10..12
 constexpr int kStoreWarps = 3;
 constexpr int kRoleThreads = 32 * (kStoreWarp0 + kStoreWarps);  // 416
+constexpr int kFirstFills = 2;     // slots filled at the start; the rest follow the first tile
 constexpr int kLookbackWidth = 5;  // one look-back pass covers 160 tiles: a round of tiles
 static_assert(kSlots % kTeams == 0 && kSlots % kSettleWarps == 0 && kSlots % kStoreWarps == 0,
               "a slot must always meet the same warps");
@@ -486,11 +487,21 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
   }
   __syncthreads();
   const unsigned long long G = gridDim.x;
+  // The first round: kFirstFills slots at once, the rest when the first tile has landed.
+  // Every CTA asks for its whole ring at the start; holding most of it back lets each CTA's
+  // first tiles arrive (and the pipeline start) well before the burst is through.
   if (tid == 0)
-    for (int s = 0; s < kSlots; ++s) fill_slot(a, sm, s, blockIdx.x + (unsigned long long)s * G);
+    for (int s = 0; s < kFirstFills; ++s) fill_slot(a, sm, s, blockIdx.x + (unsigned long long)s * G);
   if (warp < kSettleWarp0) pack_role(a, sm, status, ctl, warp / kTeamWarps, warp % kTeamWarps, lane);
   else if (warp < kStoreWarp0) settle_role(a, sm, status, tstart, ctl, warp - kSettleWarp0, lane);
-  else store_role(a, sm, ctl, warp - kStoreWarp0, lane);
+  else {
+    if (warp == kStoreWarp0 && lane == 0 && blockIdx.x < a.total_tiles &&
+        mbar_wait(&sm.full[0], 0u, a.wait_limit_ns))
+      for (int s = kFirstFills; s < kSlots; ++s)
+        fill_slot(a, sm, s, blockIdx.x + (unsigned long long)s * G);
+    __syncwarp();
+    store_role(a, sm, ctl, warp - kStoreWarp0, lane);
+  }
 }
 
 __global__ void lookback_probe_kernel(uint8_t* ws, uint64_t epoch, uint64_t limit_ns) {
@@ -549,21 +560,27 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
   args.total_tiles = tiles;
   args.hdr_words_end = hdr;
 
-  static int resident = 0;  // CTAs of this kernel that fit on the device at once
+  // CTAs of this kernel that fit on the current device at once, found once per device
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> resident_of[kMaxDevices];
   const int smem = (int)sizeof(CompressShared);
   cudaError_t e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_failure(e);
+  if (dev < 0 || dev >= kMaxDevices) return ZVC_ERR_INVALID_ARG;
+  int resident = resident_of[dev].load();
   if (resident == 0) {
     e = cudaFuncSetAttribute(compress_kernel<MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return cuda_failure(e);
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_failure(e);
+    int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_failure(e);
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel<MAXT>,
                                                            kRoleThreads, smem)) != cudaSuccess)
       return cuda_failure(e);
     resident = sms * (per_sm > 0 ? per_sm : 1);
+    resident_of[dev].store(resident);
   }
   const uint64_t grid = tiles == 0 ? 1 : (tiles < (uint64_t)resident ? tiles : (uint64_t)resident);
   cudaLaunchConfig_t cfg = {};
