@@ -7,9 +7,9 @@
 // (G = grid size) in that order, so every tile a CTA waits for belongs to a running CTA.
 // Each CTA keeps a ring of shared-memory slots; a tile's slot goes through four roles:
 //   load    a 1-D TMA bulk copy brings the tile's 16 KB into the slot, 128 words in
-//   pack    a team of 4 warps takes the tile, 32 windows each: every warp reads its
+//   pack    a team of 8 warps takes the tile, 16 windows each: every warp reads its
 //           windows' words into registers and takes a ballot per window (the window's mask);
-//           the sizes 1 + popc(mask) give each window's place, the team's 4 totals (through
+//           the sizes 1 + popc(mask) give each window's place, the team's 8 totals (through
 //           shared memory) each warp's base, and popc(mask & lanes below) each word's place
 //           inside its window. After a team barrier (every word read) the masks and non-zero
 //           words are written back into the same slot, packed from word 0. The tile's packed
@@ -62,25 +62,25 @@ __device__ __forceinline__ void put_u64_words(uint32_t* p, uint64_t v) {
 // settled by settle warp i % 2 and stored by store warp i % kStoreWarps; kSlots is a
 // multiple of all three, so a slot always meets the same warps. The slot's mbarriers:
 //   full     the TMA copy has landed (or the tile is read from global memory directly)
-//   packed   the 4 warps of the pack team have written the packed tile
+//   packed   the 8 warps of the pack team have written the packed tile
 //   settled  a settle warp has found the tile's place in the payload
 // The store warp that empties a slot starts its refill, so no barrier marks it empty.
 constexpr int kSlots = 12;
 constexpr uint32_t kInOffset = kTileWindows;                 // input lands 128 words in
 constexpr uint32_t kSlotWords = kInOffset + kTileElems;      // 4224: a dense tile's packed size
-constexpr int kTeamWarps = 4;                                // a pack team: 32 windows per warp
-constexpr int kTeams = 2;                                    // warps 0..3 and 4..7
+constexpr int kTeamWarps = 8;                                // a pack team: 16 windows per warp
+constexpr int kTeams = 2;                                    // warps 0..7 and 8..15
 constexpr uint32_t kWinPerWarp = kTileWindows / kTeamWarps;  // 32
-constexpr int kSettleWarp0 = kTeams * kTeamWarps;            // warps 8, 9
+constexpr int kSettleWarp0 = kTeams * kTeamWarps;            // warps 16, 17
 constexpr int kSettleWarps = 2;
-constexpr int kStoreWarp0 = kSettleWarp0 + kSettleWarps;     // warps 10..12
+constexpr int kStoreWarp0 = kSettleWarp0 + kSettleWarps;     // warps 18..20
 constexpr int kStoreWarps = 3;
-constexpr int kRoleThreads = 32 * (kStoreWarp0 + kStoreWarps);  // 416
+constexpr int kRoleThreads = 32 * (kStoreWarp0 + kStoreWarps);  // 672
 constexpr int kFirstFills = 2;     // slots filled at the start; the rest follow the first tile
 constexpr int kLookbackWidth = 5;  // one look-back pass covers 160 tiles: a round of tiles
 static_assert(kSlots % kTeams == 0 && kSlots % kSettleWarps == 0 && kSlots % kStoreWarps == 0,
               "a slot must always meet the same warps");
-static_assert(kWinPerWarp == 32, "one mask per lane of a pack warp");
+static_assert(kWinPerWarp * kTeamWarps == kTileWindows && kWinPerWarp <= 32, "a team covers a tile");
 
 struct SlotInfo {
   uint64_t lt;          // tile index inside its tensor
@@ -268,7 +268,7 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
     }
     const SlotInfo& f = sm.info[s];
     uint32_t* slot = sm.slot[s];
-    // read: this lane's word of each of the warp's 32 windows
+    // read: this lane's word of each of the warp's 16 windows
     uint32_t v[kWinPerWarp];
     uint32_t nwin = kTileWindows;
     if (!f.direct) {
