@@ -70,10 +70,11 @@ def parse_args(argv=None):
 # dram__bytes_read.sum + dram__bytes_write.sum of every compress (decompress) launch of
 # one timed step, captured with
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
-#       --clock-control none -k regex:^<kernel> -s 8 -c 8 --csv --log-file <csv>
+#       --clock-control none -k regex:^<kernel> -s <L> -c <L> --csv --log-file <csv>
 #       python bench.py --steps 2 --warmup 1 --no-cpu-baseline
-# (the warm-up step's 8 launches skipped, the next step's 8 captured: together they cover
-# every word of the stack once). The record holds bytes per word and the hash of the
+# with L the kernel's launches per step (one per offload segment: 6 for the AlexNet stack),
+# so that the warm-up step's launches are skipped and the next step's captured: together
+# they cover every word of the stack once. The record holds bytes per word and the hash of the
 # kernel's sources; once a source changes the record no longer applies and `traffic` is
 # null until it is captured again.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_traffic.json")
@@ -107,16 +108,27 @@ def ncu_dram_bytes(csv_path: str):
     return [per[k] for k in sorted(per, key=int)]
 
 
-def write_traffic(csvs):
+def launches_per_step(chunk_elems: int) -> int:
+    """Compress (and decompress) launches of one bench step: one per offload segment."""
+    import activation_sparsity_compression_gb300 as zvc
+    import workloads
+    ns = [c * h * w * 128 for c, h, w, _ in workloads.ALEXNET_LAYERS]
+    return sum(-(-n // zvc.zvc_offload_segment_elems(n, chunk_elems)) for n in ns)
+
+
+def write_traffic(csvs, chunk_elems):
     import workloads
     n_words = sum(c * h * w * 128 for c, h, w, _ in workloads.ALEXNET_LAYERS)
+    L = launches_per_step(chunk_elems)
     rec = {"command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
-                      "gpu__time_duration.sum --clock-control none -k regex:^<kernel> -s 8 -c 8 "
-                      "--csv --log-file <csv> python bench.py --steps 2 --warmup 1 "
+                      f"gpu__time_duration.sum --clock-control none -k regex:^<kernel> -s {L} "
+                      f"-c {L} --csv --log-file <csv> python bench.py --steps 2 --warmup 1 "
                       "--no-cpu-baseline",
            "words_per_step": n_words, "kernels": {}}
     for kernel, path in zip(("compress_kernel", "decompress_kernel"), csvs):
         b = ncu_dram_bytes(path)
+        if len(b) != L:
+            raise SystemExit(f"{path}: {len(b)} launches captured, one step has {L}")
         rec["kernels"][kernel] = {"source_sha256": kernel_source_hash(kernel), "launches": len(b),
                                   "dram_bytes": sum(b), "dram_bytes_per_word": sum(b) / n_words}
     with open(TRAFFIC_FILE, "w") as f:
@@ -807,7 +819,7 @@ def run_layouts(args):
 def main(argv=None):
     args = parse_args(argv)
     if args.write_traffic:
-        return write_traffic(args.write_traffic)
+        return write_traffic(args.write_traffic, args.chunk_elems)
     if args.train:
         return run_train(args)
     if args.layouts:
