@@ -420,7 +420,11 @@ def run_ours(args):
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "traffic_unit": "bytes per launch",
                 "algorithmic_bytes_per_launch": algo_bytes / launches,
-                "avg_launch_us": kms / launches * 1e3, "share_of_step": kms / ms}
+                "avg_launch_us": kms / launches * 1e3, "share_of_step": kms / ms,
+                # every traced kernel, for comparison with the ncu launch list's shares
+                "kernels": {f"{k}_kernel": {"launches": v[0], "ms": v[1],
+                                            "share_of_step": v[1] / ms}
+                            for k, v in trace.items()}}
 
     extra = measure_components(args, zvc, torch, xs, ns, C, dev, stream, peak)
     e2e = measure_e2e(args, zvc, torch, xs, ns, C, dev, stream, step, hsize)
