@@ -18,17 +18,19 @@
 //           records; each record start is noted in shared memory, and a second phase
 //           writes every record's header from its start and the next one's
 // Decompress: one warp per window checks the header and its table entries, stages the
-// window's records in shared memory, lets one lane walk the headers (each record's place
-// depends on every earlier one), zero-fills the window's output with coalesced stores and
-// then copies each record's literals.
+// window's records in shared memory and zero-fills the window's output with coalesced
+// stores; then, kRleBatch records at a time, one lane walks the headers (each record's place
+// depends on every earlier one) and the lanes copy the walked records' literals.
 #include "zvc_internal.cuh"
 
 namespace zvc {
 namespace {
 
 constexpr uint32_t kRleMagic = 0x31454C52u;  // "RLE1"
-constexpr uint32_t kRleWarps = 8;           // windows per CTA in sizes (and at most elsewhere)
-constexpr uint64_t kSmemBudget = 160 * 1024;  // encode / decode: shared memory per CTA
+constexpr uint32_t kRleWarps = 8;           // windows per CTA in sizes
+constexpr uint32_t kRleMaxWarps = 32;       // windows per CTA in encode / decode, at most
+constexpr uint64_t kSmemBudget = 200 * 1024;  // encode / decode: shared memory per CTA
+constexpr uint32_t kRleBatch = 128;         // records walked before their literals are copied
 constexpr uint32_t kScanThreads = 1024;
 
 __device__ __forceinline__ uint32_t lanemask_le(uint32_t lane) {
@@ -158,7 +160,7 @@ struct RecStart {
   uint32_t nz;   // non-zeros of the window before it
 };
 
-__global__ void __launch_bounds__(32 * kRleWarps)
+__global__ void __launch_bounds__(32 * kRleMaxWarps)
     rle_encode_kernel(const uint32_t* in, uint64_t n, uint32_t W, uint64_t nwin, uint32_t* out,
                       uint32_t recs_per_warp) {
   extern __shared__ __align__(16) RecStart rs_all[];
@@ -198,17 +200,11 @@ __global__ void __launch_bounds__(32 * kRleWarps)
 }
 
 // ------------------------------------------------------------------ decompress
-struct RecRun {
-  uint32_t out;   // window position of its first zero
-  uint32_t zeros;
-  uint32_t lits;
-  uint32_t src;   // staged word index of its first literal
-};
-
-__global__ void __launch_bounds__(32 * kRleWarps)
+// A walked record: x = window position of its first literal, y = literal count | staged
+// word index of its first literal << 16 (both below 2^16: W <= 4096).
+__global__ void __launch_bounds__(32 * kRleMaxWarps)
     rle_decode_kernel(const uint32_t* in, uint64_t in_bytes, uint64_t n, uint32_t W,
-                      uint64_t nwin, uint32_t* y, uint8_t* ws, uint32_t stage_words,
-                      uint32_t runs_per_warp) {
+                      uint64_t nwin, uint32_t* y, uint8_t* ws, uint32_t stage_words) {
   extern __shared__ __align__(16) uint32_t dsm[];
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint64_t w = (uint64_t)blockIdx.x * (blockDim.x >> 5) + warp;
@@ -222,8 +218,8 @@ __global__ void __launch_bounds__(32 * kRleWarps)
     }
     return;
   }
-  uint32_t* buf = dsm + (uint64_t)warp * (stage_words + 4 * runs_per_warp);
-  RecRun* runs = reinterpret_cast<RecRun*>(buf + stage_words);
+  uint32_t* buf = dsm + (uint64_t)warp * (stage_words + 2 * kRleBatch);
+  uint2* runs = reinterpret_cast<uint2*>(buf + stage_words);
   // header and this window's table entries (all lanes, same values; all in bounds once
   // in_bytes covers the header and table, which is checked first)
   const uint64_t table_end = 32 + 8 * nwin;
@@ -247,40 +243,45 @@ __global__ void __launch_bounds__(32 * kRleWarps)
     if (lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, w);
     return;
   }
-  // stage the window's records
+  // stage the window's records and zero-fill its output
   const uint32_t cnt = (uint32_t)((next - off) / 4);
   const uint32_t* src = in + table_end / 4 + off / 4;
   for (uint32_t k = lane; k < cnt; k += 32) buf[k] = __ldcs(src + k);
-  __syncwarp();
-  // walk the headers (one lane); every record covers at least one word, so at most len
-  uint32_t R = 0, good = 1;
-  if (lane == 0) {
-    uint32_t p = 0, pos = 0;
-    while (pos < len) {
-      if (p >= cnt) { good = 0; break; }
-      const uint32_t h = buf[p];
-      const uint32_t z = h & 0xFFFFu, l = h >> 16;
-      if (z + l == 0 || z + l > len - pos || p + 1 + l > cnt) { good = 0; break; }
-      runs[R++] = RecRun{pos, z, l, p + 1};
-      pos += z + l;
-      p += 1 + l;
-    }
-    if (good && p != cnt) good = 0;
-  }
-  good = __shfl_sync(0xffffffffu, good, 0);
-  R = __shfl_sync(0xffffffffu, R, 0);
-  if (!good) {
-    if (lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, w);
-    return;
-  }
-  // zero-fill the window, then place the literals record by record
   uint32_t* dst = y + begin;
   for (uint32_t k = lane; k < len; k += 32) dst[k] = 0u;
   __syncwarp();
-  for (uint32_t r = lane; r < R; r += 32) {
-    const RecRun a = runs[r];
-    for (uint32_t k = 0; k < a.lits; ++k) dst[a.out + a.zeros + k] = buf[a.src + k];
+  // walk the headers (lane 0) kRleBatch records at a time, copying each batch's literals;
+  // every record covers at least one word, so the walk ends within len records
+  uint32_t p = 0, pos = 0, good = 1;
+  while (true) {
+    uint32_t nb = 0;
+    if (lane == 0) {
+      while (nb < kRleBatch && pos < len) {
+        if (p >= cnt) { good = 0; break; }
+        const uint32_t h = buf[p];
+        const uint32_t z = h & 0xFFFFu, l = h >> 16;
+        if (z + l == 0 || z + l > len - pos || p + 1 + l > cnt) { good = 0; break; }
+        runs[nb++] = make_uint2(pos + z, l | ((p + 1) << 16));
+        pos += z + l;
+        p += 1 + l;
+      }
+    }
+    nb = __shfl_sync(0xffffffffu, nb, 0);
+    good = __shfl_sync(0xffffffffu, good, 0);
+    pos = __shfl_sync(0xffffffffu, pos, 0);
+    __syncwarp();
+    if (!good) break;
+    for (uint32_t r = lane; r < nb; r += 32) {
+      const uint2 a = runs[r];
+      const uint32_t lits = a.y & 0xFFFFu, s0 = a.y >> 16;
+      for (uint32_t k = 0; k < lits; ++k) dst[a.x + k] = buf[s0 + k];
+    }
+    __syncwarp();  // the batch's records are read before the next batch overwrites them
+    if (pos >= len) break;
   }
+  if (lane == 0 && good && p != cnt) good = 0;
+  good = __shfl_sync(0xffffffffu, good, 0);
+  if (!good && lane == 0) latch_error(ctl, ZVC_ERR_CORRUPT, w);
 }
 
 bool window_ok(uint32_t W) { return W >= 32 && W % 32 == 0 && W <= ZVC_RLE_MAX_WINDOW; }
@@ -315,7 +316,7 @@ zvc_status launch_rle_compress(const uint32_t* in, uint64_t n, uint32_t W, uint3
     const uint32_t recs = W;  // a record covers at least one word
     const uint64_t per_warp = (uint64_t)recs * sizeof(RecStart);
     uint64_t warps = kSmemBudget / per_warp;
-    warps = warps < 1 ? 1 : (warps > kRleWarps ? kRleWarps : warps);
+    warps = warps < 1 ? 1 : (warps > kRleMaxWarps ? kRleMaxWarps : warps);
     const uint64_t smem = warps * per_warp;
     cudaError_t e = cudaFuncSetAttribute(rle_encode_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -333,17 +334,16 @@ zvc_status launch_rle_decompress(const uint32_t* in, uint64_t in_bytes, uint32_t
   if (!window_ok(W)) return ZVC_ERR_INVALID_ARG;
   const uint64_t nwin = ceil_div_u64(n, W);
   const uint32_t stage_words = (uint32_t)round_up_u64(W + 1, 4);
-  const uint32_t runs = W;  // a record covers at least one word
-  const uint64_t per_warp = 4ull * (stage_words + 4ull * runs);
+  const uint64_t per_warp = 4ull * (stage_words + 2ull * kRleBatch);
   uint64_t warps = kSmemBudget / per_warp;
-  warps = warps < 1 ? 1 : (warps > kRleWarps ? kRleWarps : warps);
+  warps = warps < 1 ? 1 : (warps > kRleMaxWarps ? kRleMaxWarps : warps);
   const uint64_t smem = warps * per_warp;
   cudaError_t e = cudaFuncSetAttribute(rle_decode_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_failure(e);
   const uint64_t blocks = nwin == 0 ? 1 : ceil_div_u64(nwin, warps);
   rle_decode_kernel<<<(unsigned)blocks, (unsigned)(32 * warps), smem, stream>>>(
-      in, in_bytes, n, W, nwin, y, ws, stage_words, runs);
+      in, in_bytes, n, W, nwin, y, ws, stage_words);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_failure(e);
   return ZVC_OK;
