@@ -243,9 +243,8 @@ __device__ __forceinline__ void team_sync(uint32_t team) {
 // returns the position after it.
 __device__ __forceinline__ uint32_t pack_window(uint32_t* slot, uint32_t pos, uint32_t v,
                                                 uint32_t m, uint32_t lane, uint32_t lane_below) {
-  const uint32_t at = v != 0u ? pos + 1u + __popc(m & lane_below) : pos;
-  slot[at] = v != 0u ? v : m;
-  if (m == 0xffffffffu && lane == 0) slot[pos] = m;
+  if (v != 0u) slot[pos + 1u + __popc(m & lane_below)] = v;
+  if (lane == 0) slot[pos] = m;
   return pos + 1u + __popc(m);
 }
 
@@ -306,8 +305,9 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
       st_relaxed_u64(status + t, (a.epoch << kAggBits) | agg);  // publish the aggregate now
       sm.info[s].agg = agg;
     }
-    // write back, packed: one store per window, in which the lanes holding a zero write
-    // the mask (only a window without zeros needs a second store for it)
+    // write back, packed: per window one store of the non-zero words and one of the mask
+    // (by lane 0), which costs fewer instructions than folding the mask into the lanes
+    // holding a zero and testing every window for having none
     if (nwin == kTileWindows && !keep_woff) {
 #pragma unroll
       for (uint32_t j = 0; j < kWinPerWarp; ++j) pos = pack_window(slot, pos, v[j], m[j], lane, lane_below);
