@@ -294,13 +294,11 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
     uint32_t* tt = sm.team_tot[team][round & 1u];
     if (lane == 0) tt[q] = tot;
     team_sync(team);  // every word of the tile is read and every warp total is in
-    uint32_t pos = 0, agg = 0;
-#pragma unroll
-    for (uint32_t r = 0; r < kTeamWarps; ++r) {
-      const uint32_t x = tt[r];
-      pos += r < q ? x : 0u;
-      agg += x;
-    }
+    // lane r < kTeamWarps reads warp r's total: the warp's base and the tile's aggregate
+    const uint32_t x = lane < kTeamWarps ? tt[lane] : 0u;
+    const uint32_t pos0 = __reduce_add_sync(0xffffffffu, lane < q ? x : 0u);
+    const uint32_t agg = __reduce_add_sync(0xffffffffu, x);
+    uint32_t pos = pos0;
     if (q == 0 && lane == 0) {
       st_relaxed_u64(status + t, (a.epoch << kAggBits) | agg);  // publish the aggregate now
       sm.info[s].agg = agg;
