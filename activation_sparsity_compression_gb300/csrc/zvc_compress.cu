@@ -418,7 +418,11 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
     if (f.ok) {
       const uint32_t agg = f.agg;
       uint32_t* g = a.out + f.dst;
-      // words up to the first 16-byte boundary of the destination, then 16-byte stores
+      // words up to the first 16-byte boundary of the destination, then 16-byte stores;
+      // where the slot side is not 16-byte aligned, every lane reads the two aligned 16-byte
+      // groups its four words straddle (conflict-free, unlike four strided 4-byte loads) and
+      // picks them out. The second group may reach up to 3 words past the packed tile:
+      // still inside the shared-memory block, and those words are not used.
       const uint32_t head = min(agg, (4u - (uint32_t)((reinterpret_cast<uintptr_t>(g) >> 2) & 3u)) & 3u);
       if (lane < head) g[lane] = src[lane];
       const uint32_t nv = (agg - head) >> 2;
@@ -427,11 +431,23 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
       if (head == 0) {
 #pragma unroll 4
         for (uint32_t q = lane; q < nv; q += 32) gv[q] = sv[q];
+      } else if (head == 1) {
+#pragma unroll 4
+        for (uint32_t q = lane; q < nv; q += 32) {
+          const uint4 x = sv[q], y = sv[q + 1];
+          gv[q] = make_uint4(x.y, x.z, x.w, y.x);
+        }
+      } else if (head == 2) {
+#pragma unroll 4
+        for (uint32_t q = lane; q < nv; q += 32) {
+          const uint4 x = sv[q], y = sv[q + 1];
+          gv[q] = make_uint4(x.z, x.w, y.x, y.y);
+        }
       } else {
 #pragma unroll 4
         for (uint32_t q = lane; q < nv; q += 32) {
-          const uint32_t* p = src + head + 4 * q;
-          gv[q] = make_uint4(p[0], p[1], p[2], p[3]);
+          const uint4 x = sv[q], y = sv[q + 1];
+          gv[q] = make_uint4(x.w, y.x, y.y, y.z);
         }
       }
       const uint32_t done = head + 4 * nv;
