@@ -11,7 +11,8 @@ GB/s through that round trip with the activations already in HBM.
 The same line reports, measured in the same run:
   roofline      the dominant kernel's algorithmic bytes (4n read + S written for
                 compress, S read + 4n written for decompress) per device second, against
-                the measured HBM copy bandwidth
+                the measured HBM copy bandwidth; `kernels` lists every traced kernel's
+                launches, device time and share of the step
   compress / decompress   each kernel alone over the stack (device buffers)
   e2e           the step with inputs in pinned host memory: H2D of the inputs and D2H of
                 the restored activations inside the timed region
