@@ -503,6 +503,43 @@ def measure_components(args, zvc, torch, xs, ns, C, dev, stream, peak):
                           "hbm_gbs": reps * moved / (td / 1e3) / 1e9,
                           "hbm_frac": reps * moved / (td / 1e3) / 1e9 / peak}}
 
+    # the same stack through the batched calls: one compress launch and one decompress
+    # launch over all five layers, so the ramp and drain of a launch are paid once
+    bcap = zvc.zvc_batch_size_bound(ns, C)
+    bout = torch.empty(bcap, dtype=torch.uint8, device=dev)
+    bsize = torch.zeros(1, dtype=torch.int64, device=dev)
+    bws = zvc.new_workspace(max(zvc.zvc_batch_workspace_size(ns, C), 256), dev)
+    xptrs = [x.data_ptr() for x in xs]
+    yptrs = [y.data_ptr() for y in ys]
+
+    def bcomp():
+        if zvc.zvc_compress_batched(xptrs, ns, C, bout.data_ptr(), bcap, bsize.data_ptr(),
+                                    bws.data_ptr(), bws.numel(), sh) != zvc.ZVC_OK:
+            raise RuntimeError("zvc_compress_batched")
+
+    bcomp()
+    torch.cuda.synchronize(dev)
+    BS = int(bsize.item())
+
+    def bdecomp():
+        if zvc.zvc_decompress_batched(bout.data_ptr(), BS, yptrs, ns, C, bws.data_ptr(),
+                                      bws.numel(), sh) != zvc.ZVC_OK:
+            raise RuntimeError("zvc_decompress_batched")
+
+    bdecomp()
+    torch.cuda.synchronize(dev)
+    if zvc.zvc_get_error(bws.data_ptr(), sh) != zvc.ZVC_OK or not all(
+            torch.equal(x.view(torch.int32), y.view(torch.int32)) for x, y in zip(xs, ys)):
+        raise RuntimeError("batched round trip failed")
+    tbc = _trace(zvc, lambda: [bcomp() for _ in range(reps)])["compress"][1]
+    tbd = _trace(zvc, lambda: [bdecomp() for _ in range(reps)])["decompress"][1]
+    bmoved = 4 * N + BS
+    for key, t in (("compress_batched", tbc), ("decompress_batched", tbd)):
+        res[key] = {"gbs": reps * 4 * N / (t / 1e3) / 1e9,
+                    "hbm_gbs": reps * bmoved / (t / 1e3) / 1e9,
+                    "hbm_frac": reps * bmoved / (t / 1e3) / 1e9 / peak,
+                    "launches_per_pass": 1}
+
     # offload alone and prefetch alone (wall time on the stream, events)
     hcap = [zvc.zvc_offload_host_bound(n, C) for n in ns]
     hb = [torch.empty(c, dtype=torch.uint8, pin_memory=True) for c in hcap]
