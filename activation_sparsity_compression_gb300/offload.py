@@ -271,8 +271,9 @@ class ActivationOffload:
             self._worker = self._jobs = None
 
     def __del__(self):
-        if self._jobs is not None:
-            self._jobs.put(None)
+        jobs = getattr(self, "_jobs", None)  # absent if __init__ raised
+        if jobs is not None:
+            jobs.put(None)
 
     def _wait_offloaded(self, h):
         if h.offloaded is not None:
