@@ -60,6 +60,11 @@ def parse_args(argv=None):
                    help="ZVC and RLE compression ratios of the AlexNet stack and the VGG "
                         "conv1_2 map in NCHW, NHWC and CHWN, and RLE kernel times; prints "
                         "one JSON line and exits")
+    p.add_argument("--configs", action="store_true",
+                   help="both kernels on every input configuration (single map, AlexNet "
+                        "layers, VGG conv1_2, the 2^28-word density sweep, the 57-tensor "
+                        "GoogLeNet batch in one batched launch each way); prints one JSON "
+                        "line and exits")
     p.add_argument("--write-traffic", nargs=2, metavar=("COMPRESS_CSV", "DECOMPRESS_CSV"),
                    help="turn ncu DRAM counters of one step's launches (see TRAFFIC_FILE) "
                         "into that file, keyed by the kernels' source hashes, and exit")
@@ -674,6 +679,131 @@ def run_profile_case(args):
     return 0
 
 
+def _per_launch_ms(torch, launch, reps=10, groups=3):
+    """Mean CUDA-event time of one launch in each of `groups` groups of `reps` back-to-back
+    launches on the current stream (after one warm-up launch); returns (best, all)."""
+    launch()
+    times = []
+    for _ in range(groups):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            launch()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / reps)
+    return min(times), times
+
+
+def run_configs(args):
+    """Compress and decompress alone (device buffers, back-to-back launches) on each input
+    configuration: the single 1x64x56x56 map (L2-resident: its GB/s is an L2 figure), each
+    AlexNet layer, VGG conv1_2 at batch 64, the 2^28-word density sweep (9 densities, i.i.d.
+    and 1024-word blocks), and the 57-tensor GoogLeNet batch through one batched launch each
+    way. Every case is checked bit-exact after decompression."""
+    import torch
+
+    from activation_sparsity_compression_gb300 import build as zbuild
+    zbuild.build()
+    import activation_sparsity_compression_gb300 as zvc
+    import workloads
+
+    C = args.chunk_elems
+    peak, peak_kind = hbm_peak()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    cases = []
+
+    def record(name, ns, S, tc, td, extra=None):
+        n = sum(ns)
+        moved = 4 * n + S
+        c = {"case": name, "n_words": n, "stream_bytes": S, "ratio": 4 * n / S,
+             "compress_us": tc * 1e3, "decompress_us": td * 1e3,
+             "compress_gbs": 4 * n / (tc / 1e3) / 1e9,
+             "decompress_gbs": 4 * n / (td / 1e3) / 1e9,
+             "compress_hbm_frac": moved / (tc / 1e3) / 1e9 / peak,
+             "decompress_hbm_frac": moved / (td / 1e3) / 1e9 / peak}
+        if extra:
+            c.update(extra)
+        cases.append(c)
+        print(json.dumps(c), file=sys.stderr, flush=True)
+
+    def single(name, x, extra=None):
+        n = x.numel()
+        cap = zvc.zvc_size_bound(n, C)
+        out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+        size = torch.zeros(1, dtype=torch.int64, device="cuda")
+        ws = zvc.new_workspace(zvc.zvc_workspace_size(n, C))
+        y = torch.empty_like(x)
+
+        def comp():
+            zvc.zvc_compress(x.data_ptr(), n, C, out.data_ptr(), cap, size.data_ptr(),
+                             ws.data_ptr(), ws.numel(), sh)
+        comp()
+        torch.cuda.synchronize()
+        S = int(size.item())
+
+        def decomp():
+            zvc.zvc_decompress(out.data_ptr(), S, y.data_ptr(), n, C, ws.data_ptr(), ws.numel(), sh)
+        tc, _ = _per_launch_ms(torch, comp)
+        td, _ = _per_launch_ms(torch, decomp)
+        if zvc.zvc_get_error(ws.data_ptr(), sh) != zvc.ZVC_OK or not torch.equal(
+                x.view(torch.int32), y.view(torch.int32)):
+            raise RuntimeError(f"{name}: round trip is not bit-exact")
+        record(name, [n], S, tc, td, extra)
+        del out, y, ws
+
+    single("single_relu 1x64x56x56", workloads.single_relu(device="cuda")[0],
+           {"note": "803 KB: L2-resident, so its GB/s are L2 figures"})
+    for l, x in enumerate(workloads.alexnet_stack(device="cuda")):
+        cc, hh, ww, d = workloads.ALEXNET_LAYERS[l]
+        single(f"alexnet layer {l} 128x{cc}x{hh}x{ww} ({int(d * 100)}% non-zero)", x)
+    torch.cuda.empty_cache()
+    single("vgg_conv12 64x64x224x224", workloads.vgg_conv12(device="cuda")[0])
+    torch.cuda.empty_cache()
+    for structure in ("iid", "block"):
+        for d in workloads.SWEEP_DENSITIES:
+            x = workloads.density_sweep(d, structure, device="cuda")[0]
+            single(f"sweep 2^28 {structure} {d:.2f}", x, {"density": d, "structure": structure})
+            del x
+            torch.cuda.empty_cache()
+
+    # the GoogLeNet batch: one batched launch each way over all 57 tensors
+    xs = workloads.googlenet_batch(device="cuda")
+    ns = [x.numel() for x in xs]
+    cap = zvc.zvc_batch_size_bound(ns, C)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    size = torch.zeros(1, dtype=torch.int64, device="cuda")
+    ws = zvc.new_workspace(max(zvc.zvc_batch_workspace_size(ns, C), 256))
+    ys = [torch.empty_like(x) for x in xs]
+    xp, yp = [x.data_ptr() for x in xs], [y.data_ptr() for y in ys]
+
+    def bcomp():
+        zvc.zvc_compress_batched(xp, ns, C, out.data_ptr(), cap, size.data_ptr(), ws.data_ptr(),
+                                 ws.numel(), sh)
+    bcomp()
+    torch.cuda.synchronize()
+    S = int(size.item())
+
+    def bdecomp():
+        zvc.zvc_decompress_batched(out.data_ptr(), S, yp, ns, C, ws.data_ptr(), ws.numel(), sh)
+    tc, _ = _per_launch_ms(torch, bcomp, reps=3)
+    td, _ = _per_launch_ms(torch, bdecomp, reps=3)
+    if zvc.zvc_get_error(ws.data_ptr(), sh) != zvc.ZVC_OK or not all(
+            torch.equal(x.view(torch.int32), y.view(torch.int32)) for x, y in zip(xs, ys)):
+        raise RuntimeError("googlenet batch: round trip is not bit-exact")
+    record("googlenet batch, 57 tensors, one batched launch each way", ns, S, tc, td,
+           {"tensors": len(ns)})
+
+    print(json.dumps({"metric": "ZVC compress/decompress per input configuration",
+                      "unit": "GB/s (uncompressed) and fraction of HBM", "peak": peak,
+                      "peak_kind": peak_kind, "chunk_elems": C, "data": "synthetic",
+                      "timing": "CUDA events, one warm-up launch, best of 3 groups of "
+                                "back-to-back launches (10, or 3 for the batch)",
+                      "cases": cases}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ training step with offload
 TRAIN_MODEL = ("deep CNN: conv 3->128 (3x3, stride 2) + ReLU, then 12 x (conv 128->128 3x3 + "
                "ReLU) at 112x112, global average pool, linear 128->1000; batch 64, 3x224x224, "
@@ -862,6 +992,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.write_traffic:
         return write_traffic(args.write_traffic, args.chunk_elems)
+    if args.configs:
+        return run_configs(args)
     if args.train:
         return run_train(args)
     if args.layouts:
