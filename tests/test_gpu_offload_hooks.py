@@ -72,3 +72,43 @@ def test_retained_graph_can_be_unpacked_twice():
     for a, p in zip(first, model.parameters()):
         assert torch.equal(a, p.grad)
     off.check_errors()
+
+
+@pytest.mark.parametrize("max_pending", [0, 1, 4])
+def test_worker_queue_depth_keeps_gradients_identical(max_pending):
+    """Host mode offloads on a worker thread with at most max_pending tensors queued; the
+    depth changes only how far the training loop runs ahead, never the result."""
+    ensure_lib()
+    torch.backends.cudnn.deterministic = True
+    torch.backends.cudnn.benchmark = False
+    model = _cnn()
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = torch.randn(8, 3, 64, 64, device="cuda", generator=g)
+    ref = _step(model, x, None)
+    off = ActivationOffload(where="host", min_elems=1024, max_pending=max_pending)
+    for _ in range(2):
+        got = _step(model, x, off)
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
+    off.check_errors()
+    off.close()
+    assert off._worker is None
+
+
+def test_worker_failure_surfaces_on_unpack():
+    """An offload that fails on the worker thread raises when autograd unpacks the tensor,
+    on the training loop's thread."""
+    ensure_lib()
+    model = _cnn()
+    x = torch.randn(2, 3, 64, 64, device="cuda")
+    off = ActivationOffload(where="host", min_elems=1024)
+
+    def broken(h, t, produced, cap):
+        raise RuntimeError("planted offload failure")
+
+    off._offload_one = broken
+    with off:
+        loss = model(x).square().sum()
+    with pytest.raises(RuntimeError, match="planted offload failure"):
+        loss.backward()
+    off.close()
