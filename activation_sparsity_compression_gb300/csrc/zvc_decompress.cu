@@ -12,9 +12,10 @@
 //             bulk copy (plain loads for the unaligned ends), at their 16-byte phase
 //   walk      a window's position depends on every earlier mask, so one lane walks the
 //             masks (position += 1 + popc(mask)), recording each window's (first value,
-//             mask) and publishing how many windows are recorded every 16 windows; the
-//             walk must end exactly at the next chunk's offset
-// The scatterer expands windows as soon as they are recorded, so with two warps the
+//             mask) in one 8-byte store into a table that starts cleared; the walk must
+//             end exactly at the next chunk's offset
+// The scatterer expands windows as soon as it reads their entries non-zero, so with two
+// warps the
 // scatter runs under the walk: lane l expands words 4(l mod 8) .. +3 of window l/8 + 4k of each
 // group of 16 windows, a set bit at position b reading packed word popc(mask & (2^b - 1)),
 // a clear bit writing 0, with 16-byte stores.
@@ -29,11 +30,11 @@ namespace {
 // for the 16-byte phase), then the window table (first value, mask) per window.
 struct DecompressCtl {
   uint64_t full;        // mbarrier of the TMA copy
-  uint32_t progress;    // windows recorded in the table so far
+  uint32_t progress;    // 1 once the chunk is staged
   uint32_t state;       // 0 running, 1 walked and checked, 2 give up (nothing more to do)
 };
 constexpr uint32_t kCtlWords = 4;       // sizeof(DecompressCtl) / 4
-constexpr uint32_t kPublishEvery = 16;  // the walker publishes its progress every 16 windows
+constexpr uint32_t kPublishEvery = 16;  // the scatterer expands 16 windows at a time
 
 template <int MAXT>
 struct DecompressArgs {
@@ -177,13 +178,14 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
   }
   if (lane < head) buf[lane] = __ldcs(cw + lane);
   if (lane < tail) buf[head + body + lane] = __ldcs(cw + head + body + lane);
-  __threadfence_block();  // the end words are published with the walker's progress
+  __threadfence_block();  // the end words are published with the staged flag
   __syncwarp();
   if (body > 0 && !mbar_wait(&ctl.full, 0, a.wait_limit_ns)) {
     give_up(ZVC_ERR_TIMEOUT);
     return;
   }
   __syncwarp();
+  if (lane == 0) st_release_cta(&ctl.progress, 1u);  // staged: the scatterer may read the chunk
 
   // ---- walk the masks. The chain position -> mask -> next position is the critical
   // path. A window spans at most 33 words, so the k-th read sits below 33k <= buf_words -
@@ -191,17 +193,17 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
   // grow, ending exactly at len proves that every read was inside the chunk. (For a
   // corrupt chunk the scatterer may already have expanded windows from wrong positions;
   // the output is then unspecified, but every access stays inside the buffers.)
+  // Each window's (first value, mask) goes out in one 8-byte store; the first value is never
+  // 0, and the table starts cleared, so the scatterer takes an entry once it reads non-zero:
+  // no release per group of windows holds up the walk.
   if (lane == 0) {
     uint32_t pos = 0, m = 0;
-    for (uint32_t w0 = 0; w0 < nwin; w0 += kPublishEvery) {
-      const uint32_t w1 = min(nwin, w0 + kPublishEvery);
+    unsigned long long* wm = reinterpret_cast<unsigned long long*>(wmeta);
 #pragma unroll 4
-      for (uint32_t w = w0; w < w1; ++w) {
-        m = buf[pos];
-        wmeta[w] = make_uint2(phase + pos + 1u, m);  // first value, from the buffer's start
-        pos += 1u + __popc(m);
-      }
-      st_release_cta(&ctl.progress, w1);
+    for (uint32_t w = 0; w < nwin; ++w) {
+      m = buf[pos];
+      wm[w] = (unsigned long long)(phase + pos + 1u) | ((unsigned long long)m << 32);
+      pos += 1u + __popc(m);
     }
     const uint32_t ragged = count & (kWindow - 1);
     const bool good = (pos == len) & (ragged == 0 || (m >> ragged) == 0u);
@@ -235,31 +237,44 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
   const bool vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
   const uint32_t e = 4u * (lane & 7u);
   const uint32_t below = (1u << e) - 1u;
-  uint32_t ready = 0;
   uint64_t t0 = 0;
+  // bounded wait for the walker; false: give up (the walker gave up, or the wait ran out)
+  auto waited = [&]() -> bool {
+    if (ld_acquire_cta(&ctl.state) == 2u) return false;
+    const uint64_t now = globaltimer_ns();
+    if (t0 == 0) t0 = now;
+    if (now - t0 > a.wait_limit_ns) {
+      if (lane == 0) latch_error(ec, ZVC_ERR_TIMEOUT, item);
+      return false;
+    }
+    __nanosleep(32);
+    return true;
+  };
+  while (ld_acquire_cta(&ctl.progress) == 0u)  // the chunk is staged
+    if (!waited()) return;
+  const volatile unsigned long long* wm = reinterpret_cast<const volatile unsigned long long*>(wmeta);
   for (uint32_t g0 = 0; g0 < nwin; g0 += kPublishEvery) {
     const uint32_t need = min(nwin, g0 + kPublishEvery);
-    // wait (bounded) until the walker has recorded this group, or gave up
-    while (ready < need) {
-      ready = ld_acquire_cta(&ctl.progress);
-      if (ready >= need) break;
-      if (ld_acquire_cta(&ctl.state) == 2u) return;
-      const uint64_t now = globaltimer_ns();
-      if (t0 == 0) t0 = now;
-      if (now - t0 > a.wait_limit_ns) {
-        if (lane == 0) latch_error(ec, ZVC_ERR_TIMEOUT, item);
-        return;
+    // the group's windows: lane group l/8 takes windows g0 + l/8 + 4k, k = 0..3; each lane
+    // waits (bounded) until the walker has recorded its windows
+    unsigned long long ent[4];
+    while (true) {
+      bool all = true;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w = g0 + (lane >> 3) + 4u * k;
+        ent[k] = w < need ? wm[w] : 1ull;
+        all &= (uint32_t)ent[k] != 0u;
       }
-      __nanosleep(64);
+      if (__all_sync(0xffffffffu, all)) break;
+      if (!waited()) return;
     }
-    // the group's windows: lane group l/8 takes windows g0 + l/8 + 4k, k = 0..3
     uint4 r[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t w = g0 + (lane >> 3) + 4u * k;
-      const uint2 mo = w < need ? wmeta[w] : make_uint2(0u, 0u);
-      const uint32_t m = mo.y;
-      uint32_t q = mo.x + __popc(m & below);
+      const uint32_t m = w < need ? (uint32_t)(ent[k] >> 32) : 0u;
+      uint32_t q = (uint32_t)ent[k] + __popc(m & below);
       uint32_t v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -307,6 +322,11 @@ __global__ void __launch_bounds__(kMaxThreads)
     fence_mbar_init();
     ctl.progress = 0;
     ctl.state = 0;
+  }
+  // the window tables start cleared: an entry is taken once it reads non-zero
+  for (uint32_t c2 = 0; c2 < a.chunks_per_cta; ++c2) {
+    uint32_t* wz = dsm_all + (uint64_t)c2 * a.slot_words + kCtlWords + a.meta_offset_words;
+    for (uint32_t i = threadIdx.x; i < 2u * (a.chunk_elems / kWindow); i += blockDim.x) wz[i] = 0u;
   }
   __syncthreads();
   if (item >= a.total_items) return;
