@@ -29,12 +29,31 @@ namespace {
 // Shared memory of a CTA: control words, then the chunk buffer (C/32 masks + C words, +3
 // for the 16-byte phase), then the window table (first value, mask) per window.
 struct DecompressCtl {
-  uint64_t full;        // mbarrier of the TMA copy
-  uint32_t progress;    // 1 once the chunk is staged
-  uint32_t state;       // 0 running, 1 walked and checked, 2 give up (nothing more to do)
+  uint64_t full;      // mbarrier of the TMA copies, one phase per bulk copy
+  uint32_t progress;  // pieces of the chunk staged so far
+  uint32_t state;     // 0 running, 1 walked and checked, 2 give up (nothing more to do)
+  uint32_t drain;     // 0, or the window the next piece starts at (walker -> scatterer)
+  uint32_t expanded;  // the windows before it are read out of the buffer (scatterer -> walker)
+  uint32_t pad[2];
 };
-constexpr uint32_t kCtlWords = 4;       // sizeof(DecompressCtl) / 4
+constexpr uint32_t kCtlWords = 8;       // sizeof(DecompressCtl) / 4, keeps the buffer 16-byte aligned
+static_assert(sizeof(DecompressCtl) == 4 * kCtlWords, "control words");
 constexpr uint32_t kPublishEvery = 16;  // the scatterer expands 16 windows at a time
+constexpr uint32_t kPollSleepNs = 32;   // the scatterer's sleep between polls of the table
+constexpr uint32_t kStageSuspendNs = 2000;  // the scatterer's barrier wait for the first piece
+
+// mbarrier.try_wait with a suspend hint of HINT ns.
+template <uint32_t HINT>
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "n"(HINT)
+      : "memory");
+  return done != 0;
+}
 
 template <int MAXT>
 struct DecompressArgs {
@@ -47,7 +66,7 @@ struct DecompressArgs {
   uint32_t chunk_elems;
   uint32_t T;
   uint32_t batched;
-  uint32_t buf_words;          // largest valid chunk: C/32 masks + C words
+  uint32_t cap_words;          // chunk buffer words (a multiple of 4): longer chunks go in pieces
   uint32_t meta_offset_words;  // window table, 8-byte aligned
   uint32_t chunks_per_cta;
   uint32_t solo;               // 1: one warp walks and then scatters its chunk
@@ -164,52 +183,130 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
 
   // ---- stage the chunk: its words sit in shared memory at the same 16-byte phase as in
   // global memory, so one bulk copy moves the aligned body; lanes load the at most three
-  // words on either side.
+  // words on either side. The buffer holds cap words; a longer chunk is staged in pieces
+  // (below), the first piece being its first cap - phase words.
   const uint32_t len = (uint32_t)((end - start) / 4);
   const uint32_t* cw = sw + kStreamHeaderWords + 2 * nc + start / 4;
-  const uint32_t phase = (uint32_t)((reinterpret_cast<uintptr_t>(cw) >> 2) & 3u);
-  buf += phase;
-  const uint32_t head = min(len, (4u - phase) & 3u);
-  const uint32_t body = (len - head) & ~3u;
-  const uint32_t tail = len - head - body;
-  if (body > 0 && lane == 0) {
-    mbar_arrive_expect_tx(&ctl.full, body * 4);
-    bulk_g2s(buf + head, cw + head, body * 4, &ctl.full);
+  const uint32_t cap = a.cap_words;
+  uint32_t ph = (uint32_t)((reinterpret_cast<uintptr_t>(cw) >> 2) & 3u);
+  uint32_t e = min(len, cap - ph);  // chunk words [s, e) are staged, s = 0 here
+  uint32_t fills = 0;                // bulk copies completed on ctl.full (its phase)
+  {
+    const uint32_t head = min(e, (4u - ph) & 3u);
+    const uint32_t body = (e - head) & ~3u;
+    const uint32_t tail = e - head - body;
+    if (body > 0 && lane == 0) {
+      mbar_arrive_expect_tx(&ctl.full, body * 4);
+      bulk_g2s(buf + ph + head, cw + head, body * 4, &ctl.full);
+    }
+    if (lane < head) buf[ph + lane] = __ldcs(cw + lane);
+    if (lane < tail) buf[ph + head + body + lane] = __ldcs(cw + head + body + lane);
+    __threadfence_block();  // the end words are published with the staged count
+    __syncwarp();
+    if (body > 0 && !mbar_wait(&ctl.full, 0, a.wait_limit_ns)) {
+      give_up(ZVC_ERR_TIMEOUT);
+      return;
+    }
+    fills = body > 0 ? 1u : 0u;
+    __syncwarp();
   }
-  if (lane < head) buf[lane] = __ldcs(cw + lane);
-  if (lane < tail) buf[head + body + lane] = __ldcs(cw + head + body + lane);
-  __threadfence_block();  // the end words are published with the staged flag
-  __syncwarp();
-  if (body > 0 && !mbar_wait(&ctl.full, 0, a.wait_limit_ns)) {
-    give_up(ZVC_ERR_TIMEOUT);
-    return;
-  }
-  __syncwarp();
-  if (lane == 0) st_release_cta(&ctl.progress, 1u);  // staged: the scatterer may read the chunk
+  if (lane != 0) return;
+  st_release_cta(&ctl.progress, 1u);  // staged: the scatterer may read the piece
 
   // ---- walk the masks. The chain position -> mask -> next position is the critical
-  // path. A window spans at most 33 words, so the k-th read sits below 33k <= buf_words -
-  // 33 and stays in this CTA's buffer even for a corrupt chunk, and since positions only
-  // grow, ending exactly at len proves that every read was inside the chunk. (For a
-  // corrupt chunk the scatterer may already have expanded windows from wrong positions;
-  // the output is then unspecified, but every access stays inside the buffers.)
+  // path. A window spans at most 33 words, so from buffer position bp the next
+  // (cap - bp) / 33 windows lie inside the buffer and are walked without checks; the rest
+  // one by one. Inside the buffer means staged, except in the chunk's last piece, where
+  // only a corrupt chunk reads past its end: positions only grow, so ending exactly at len
+  // proves that every read was inside the chunk. (For a corrupt chunk the scatterer may
+  // already have expanded windows from wrong positions; the output is then unspecified,
+  // but every access stays inside the buffers.)
   // Each window's (first value, mask) goes out in one 8-byte store; the first value is never
   // 0, and the table starts cleared, so the scatterer takes an entry once it reads non-zero:
   // no release per group of windows holds up the walk.
-  if (lane == 0) {
-    uint32_t pos = 0, m = 0;
-    unsigned long long* wm = reinterpret_cast<unsigned long long*>(wmeta);
+  // A window that runs past the buffer before the chunk's end starts the next piece: the
+  // walker asks the scatterer to expand every window recorded so far (drain), waits until
+  // it has, and stages the chunk from that window on.
+  unsigned long long* wm = reinterpret_cast<unsigned long long*>(wmeta);
+  uint32_t s = 0, bp = ph, m = 0, w = 0, piece = 1;
+  bool good = true;
+  while (w < nwin) {
+    const uint32_t k = min(nwin - w, (cap - bp) / (kWindow + 1));
+    if (k > 0) {
+      const uint32_t w1 = w + k;
 #pragma unroll 4
-    for (uint32_t w = 0; w < nwin; ++w) {
-      m = buf[pos];
-      wm[w] = (unsigned long long)(phase + pos + 1u) | ((unsigned long long)m << 32);
-      pos += 1u + __popc(m);
+      for (; w < w1; ++w) {
+        m = buf[bp];
+        wm[w] = (unsigned long long)(bp + 1u) | ((unsigned long long)m << 32);
+        bp += 1u + __popc(m);
+      }
+      continue;
     }
-    const uint32_t ragged = count & (kWindow - 1);
-    const bool good = (pos == len) & (ragged == 0 || (m >> ragged) == 0u);
-    if (!good) latch_error(ec, ZVC_ERR_CORRUPT, item);
-    st_release_cta(&ctl.state, good ? 1u : 2u);
+    if (bp < cap) {
+      m = buf[bp];
+      const uint32_t nb = bp + 1u + __popc(m);
+      if (nb <= cap) {
+        wm[w] = (unsigned long long)(bp + 1u) | ((unsigned long long)m << 32);
+        bp = nb;
+        ++w;
+        continue;
+      }
+    }
+    // the window runs past the buffer: past the chunk in its last piece (corrupt), else
+    // the next piece starts at this window
+    if (e >= len || a.solo) {
+      good = false;
+      break;
+    }
+    const uint32_t pos = s + (bp - ph);
+    st_release_cta(&ctl.drain, w);
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_cta(&ctl.expanded) != w) {
+      if (globaltimer_ns() - t0 > a.wait_limit_ns) {
+        latch_error(ec, ZVC_ERR_TIMEOUT, item);
+        st_release_cta(&ctl.state, 2u);
+        return;
+      }
+      __nanosleep(64);
+    }
+    fence_proxy_async_smem();  // the scatterer's reads come before the copy's writes
+    // The piece starts at this window's 16-byte group: the at most three words before it
+    // are the stream's (a chunk is preceded by the header and table at least), so one bulk
+    // copy moves every whole group that fits; a piece that reaches the chunk's end loads
+    // the words past its last group with plain loads, under the copy.
+    s = pos;
+    ph = (uint32_t)((reinterpret_cast<uintptr_t>(cw + s) >> 2) & 3u);
+    const uint32_t* src = cw + s - ph;                // 16-byte aligned
+    const uint32_t n = min(len - s + ph, cap);        // words of this piece, from src
+    const uint32_t body = n & ~3u;                    // cap is a multiple of 4
+    const uint32_t rest = n - body;                   // only at the chunk's end: <= 3
+    e = s - ph + n;
+    uint32_t x[3];
+#pragma unroll
+    for (uint32_t i = 0; i < 3; ++i) x[i] = i < rest ? __ldcs(src + body + i) : 0u;
+    if (body > 0) {
+      mbar_arrive_expect_tx(&ctl.full, body * 4);
+      bulk_g2s(buf, src, body * 4, &ctl.full);
+    }
+#pragma unroll
+    for (uint32_t i = 0; i < 3; ++i)
+      if (i < rest) buf[body + i] = x[i];
+    if (body > 0) {
+      if (!mbar_wait(&ctl.full, fills & 1u, a.wait_limit_ns)) {
+        latch_error(ec, ZVC_ERR_TIMEOUT, item);
+        st_release_cta(&ctl.state, 2u);
+        return;
+      }
+      ++fills;
+    }
+    ++piece;
+    st_release_cta(&ctl.progress, piece);
+    bp = ph;
   }
+  const uint32_t ragged = count & (kWindow - 1);
+  good = good & (s + (bp - ph) == len) & (ragged == 0 || (m >> ragged) == 0u);
+  if (!good) latch_error(ec, ZVC_ERR_CORRUPT, item);
+  st_release_cta(&ctl.state, good ? 1u : 2u);
 }
 
 // Warp 1: expands the recorded windows of its chunk as the walker records them.
@@ -239,7 +336,7 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
   const uint32_t below = (1u << e) - 1u;
   uint64_t t0 = 0;
   // bounded wait for the walker; false: give up (the walker gave up, or the wait ran out)
-  auto waited = [&]() -> bool {
+  auto waited = [&](uint32_t sleep_ns) -> bool {
     if (ld_acquire_cta(&ctl.state) == 2u) return false;
     const uint64_t now = globaltimer_ns();
     if (t0 == 0) t0 = now;
@@ -247,33 +344,50 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
       if (lane == 0) latch_error(ec, ZVC_ERR_TIMEOUT, item);
       return false;
     }
-    __nanosleep(32);
+    __nanosleep(sleep_ns);
     return true;
   };
-  while (ld_acquire_cta(&ctl.progress) == 0u)  // the chunk is staged
-    if (!waited()) return;
+  uint32_t piece = 1;  // the piece of the chunk in the buffer
+  // The first piece: a hardware wait on the bulk copy's barrier (the warp sleeps until the
+  // copy lands), then the walker's staged count, which also covers its plain loads. A
+  // chunk too short for a bulk copy, or a walker that gave up, ends the barrier wait at
+  // the suspend hint.
+  while (ld_acquire_cta(&ctl.progress) < piece) {
+    if (mbar_try_wait_hint<kStageSuspendNs>(&ctl.full, 0u)) {
+      while (ld_acquire_cta(&ctl.progress) < piece)
+        if (!waited(16)) return;
+      break;
+    }
+    if (!waited(0)) return;
+  }
   const volatile unsigned long long* wm = reinterpret_cast<const volatile unsigned long long*>(wmeta);
-  for (uint32_t g0 = 0; g0 < nwin; g0 += kPublishEvery) {
+  const volatile uint32_t* drain = &ctl.drain;
+  uint32_t g0 = 0, handled = 0;
+  while (g0 < nwin) {
     const uint32_t need = min(nwin, g0 + kPublishEvery);
     // the group's windows: lane group l/8 takes windows g0 + l/8 + 4k, k = 0..3; each lane
-    // waits (bounded) until the walker has recorded its windows
+    // waits (bounded) until the walker has recorded its windows, or until the walker asks
+    // for the windows before d to be expanded (it stages the next piece from window d)
     unsigned long long ent[4];
+    uint32_t lim, d;
     while (true) {
+      d = *drain;
+      lim = (d > handled && d <= need) ? d : need;
       bool all = true;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t w = g0 + (lane >> 3) + 4u * k;
-        ent[k] = w < need ? wm[w] : 1ull;
+        ent[k] = w < lim ? wm[w] : 1ull;
         all &= (uint32_t)ent[k] != 0u;
       }
       if (__all_sync(0xffffffffu, all)) break;
-      if (!waited()) return;
+      if (!waited(kPollSleepNs)) return;
     }
     uint4 r[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t w = g0 + (lane >> 3) + 4u * k;
-      const uint32_t m = w < need ? (uint32_t)(ent[k] >> 32) : 0u;
+      const uint32_t m = w < lim ? (uint32_t)(ent[k] >> 32) : 0u;
       uint32_t q = (uint32_t)ent[k] + __popc(m & below);
       uint32_t v[4];
 #pragma unroll
@@ -287,7 +401,7 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t w = g0 + (lane >> 3) + 4u * k;
-      if (w >= need) break;
+      if (w >= lim) break;
       const uint32_t base = w * kWindow + e;
       if (vec && base + 4u <= count) {
         *reinterpret_cast<uint4*>(dst + base) = r[k];
@@ -298,6 +412,16 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
           if (base + j < count) dst[base + j] = vv[j];
       }
     }
+    g0 = lim;
+    if (lim == d && d > handled) {
+      // every window before d is read out of the buffer: hand it back, wait for the next piece
+      handled = d;
+      ++piece;
+      __syncwarp();
+      if (lane == 0) st_release_cta(&ctl.expanded, d);
+      while (ld_acquire_cta(&ctl.progress) < piece)
+        if (!waited(64)) return;
+    }
   }
 }
 
@@ -305,6 +429,10 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
 // expands it, and 8 chunks share a CTA; a larger chunk gets a walker and a scatterer warp
 // and a CTA of its own.
 constexpr uint32_t kSoloChunksPerCta = 8;
+// Buffer of a CTA with a chunk over 2048 words: 5/4 of the mean chunk + 64 words, at least
+// 1024 words (a piece then holds at least 31 windows).
+constexpr uint64_t kCapSlackNum = 5, kCapSlackDen = 4, kCapExtraWords = 64;
+constexpr uint32_t kCapMinWords = 1024;
 constexpr uint32_t kMaxThreads = 256;
 
 template <int MAXT>
@@ -322,6 +450,8 @@ __global__ void __launch_bounds__(kMaxThreads)
     fence_mbar_init();
     ctl.progress = 0;
     ctl.state = 0;
+    ctl.drain = 0;
+    ctl.expanded = 0;
   }
   // the window tables start cleared: an entry is taken once it reads non-zero
   for (uint32_t c2 = 0; c2 < a.chunks_per_cta; ++c2) {
@@ -363,15 +493,30 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   args.total_chunks = chunks;
   args.total_items = chunks + (batched && T == 0 ? 1 : T);
   const uint32_t wpc = C / kWindow;
-  args.buf_words = wpc + C;
-  args.meta_offset_words = (uint32_t)round_up_u64(args.buf_words + 4, 2);
-  args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.meta_offset_words + 2ull * wpc, 4);
+  // the largest valid chunk (C/32 masks + C words) at any 16-byte phase
+  const uint32_t full_cap = (uint32_t)round_up_u64(wpc + C + 3ull, 4);
   args.solo = C <= 2048 ? 1u : 0u;
+  args.cap_words = full_cap;
+  if (!args.solo && chunks > 0) {
+    // A CTA's shared memory is fixed at launch and sets how many chunks are in flight per
+    // SM, so the buffer is sized from the mean chunk length (the stream's size less its
+    // headers and tables): chunks up to kCapSlack times the mean go in one piece.
+    const uint64_t fixed = (batched ? 16ull + 8ull * ((uint64_t)T + 1) : 0ull) + 32ull * T +
+                           8ull * chunks;
+    const uint64_t mean = min((uint64_t)full_cap, in_bytes > fixed ? (in_bytes - fixed) / 4 / chunks : 0);
+    const uint64_t want = round_up_u64(mean * kCapSlackNum / kCapSlackDen + kCapExtraWords, 4);
+    args.cap_words = (uint32_t)min((uint64_t)full_cap, max((uint64_t)kCapMinWords, want));
+  }
+  args.meta_offset_words = args.cap_words;
+  args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.cap_words + 2ull * wpc, 4);
   args.chunks_per_cta = args.solo ? kSoloChunksPerCta : 1u;
   const uint32_t threads = args.solo ? 32u * kSoloChunksPerCta : 64u;
   const uint64_t smem = 4ull * args.slot_words * args.chunks_per_cta;
   cudaError_t e = cudaFuncSetAttribute(decompress_kernel<MAXT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_failure(e);
+  e = cudaFuncSetAttribute(decompress_kernel<MAXT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           100);
   if (e != cudaSuccess) return cuda_failure(e);
   const uint64_t blocks = ceil_div_u64(args.total_items, args.chunks_per_cta);
   const TraceMark mark = trace_begin(kTraceDecompress, stream);

@@ -47,6 +47,42 @@ def test_random_corruption_agrees_with_oracle():
     assert seen[zvc.ZVC_ERR_CORRUPT] > 50 and seen[zvc.ZVC_OK] > 10
 
 
+def test_corrupt_chunks_staged_in_pieces_agree_with_oracle():
+    """Flipped bits in dense chunks among empty ones, whose decompression is staged in
+    several pieces (the CTA buffer is sized from the mean chunk): the status and, when the
+    stream still decodes, the words must be the oracle's."""
+    ensure_lib()
+    rng = np.random.default_rng(25)
+    C = 4096
+    seen = {zvc.ZVC_OK: 0, zvc.ZVC_ERR_CORRUPT: 0}
+    for trial in range(120):
+        dens = [0.0] * 10 + [1.0, float(rng.random()), 1.0] + [0.0] * 10
+        w = np.concatenate([_rand(rng, C, d) for d in dens])
+        n = w.size - int(rng.integers(0, 100))
+        w = w[:n]
+        s = oracle.encode(w, C)
+        table_end = 32 + 8 * (-(-n // C))
+        starts = np.frombuffer(s[32:table_end].tobytes(), "<u8").astype(np.int64)
+        lo, hi = table_end + int(starts[10]), table_end + int(starts[13])  # the dense chunks
+        t = s.copy()
+        for _ in range(int(rng.integers(1, 3))):
+            if rng.random() < 0.5:  # a mask of chunk 10 or 12 (all windows full: 33 words)
+                c = int(rng.choice([10, 12]))
+                i = table_end + int(starts[c]) + 4 * 33 * int(rng.integers(0, C // 32))
+                i += int(rng.integers(0, 4))
+            else:
+                i = int(rng.integers(lo, hi))
+            t[i] ^= np.uint8(1 << int(rng.integers(0, 8)))
+        ost, owords = oracle.decode(t, n, C)
+        gst, gwords = _gpu_status(t, n, C)
+        if ost == oracle.OK:
+            assert gst == zvc.ZVC_OK and np.array_equal(gwords, owords), trial
+        else:
+            assert gst == zvc.ZVC_ERR_CORRUPT, (trial, ost, gst)
+        seen[gst] += 1
+    assert seen[zvc.ZVC_ERR_CORRUPT] > 20 and seen[zvc.ZVC_OK] > 5, seen
+
+
 def test_size_and_parameter_mismatches():
     rng = np.random.default_rng(22)
     w = _rand(rng, 50_000, 0.4)

@@ -94,6 +94,43 @@ def test_unaligned_source_and_output(off):
     assert st == zvc.ZVC_OK and err == zvc.ZVC_OK and np.array_equal(back, w)
 
 
+def _chunkwise_words(rng, C, densities):
+    return np.concatenate([_random_words(rng, C, d) for d in densities])
+
+
+CHUNK_PATTERNS = ([0.0] * 30 + [1.0] + [0.0] * 30, [1.0] + [0.0] * 40, [0.0] * 40 + [1.0],
+                  [0.0, 0.9, 0.0, 0.3, 1.0, 0.0, 0.0, 0.6] * 4, [0.05] * 20 + [0.97, 1.0])
+
+
+@pytest.mark.parametrize("C", [4096, 16384])
+def test_chunks_longer_than_the_mean(C):
+    """Dense chunks among sparse ones. A decompressing CTA's chunk buffer is sized from the
+    stream's mean chunk, so these chunks are staged and walked in several pieces, each
+    starting at a window of its own 16-byte phase."""
+    rng = np.random.default_rng(C + 7)
+    for pattern in CHUNK_PATTERNS:
+        w = _chunkwise_words(rng, C, pattern)
+        for cut in (0, 37, C // 2 + 5):
+            _assert_parity(w[:w.size - cut], C)
+
+
+@pytest.mark.parametrize("off", [1, 2, 3])
+def test_chunks_longer_than_the_mean_unaligned(off):
+    rng = np.random.default_rng(30 + off)
+    w = _chunkwise_words(rng, 4096, [0.0] * 12 + [1.0, 0.8] + [0.0] * 12)
+    n = w.size
+    s = oracle.encode(w, 4096)
+    # the stream at a 4-byte offset from 16-byte alignment, so every piece's phase moves
+    raw = torch.zeros(s.size + 16, dtype=torch.uint8, device="cuda")
+    raw[4 * off:4 * off + s.size] = torch.from_numpy(s.copy()).cuda()
+    out = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+    ws = zvc.new_workspace(zvc.ZVC_WORKSPACE_ALIGN)
+    st = zvc.zvc_decompress(raw.data_ptr() + 4 * off, s.size, out.data_ptr(), n, 4096,
+                            ws.data_ptr(), ws.numel(), sh())
+    assert st == zvc.ZVC_OK and zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), w)
+
+
 def test_single_relu_config_bit_exact():
     x = workloads.single_relu(device="cuda")[0]
     w = words_of(x)
