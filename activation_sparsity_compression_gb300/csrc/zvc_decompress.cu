@@ -21,6 +21,8 @@
 // a clear bit writing 0, with 16-byte stores.
 // Extra work items (one per tensor, after the chunks) check the headers of streams that
 // have no chunks; an empty batch gets one item that checks its header and table.
+#include <atomic>
+
 #include "zvc_internal.cuh"
 
 namespace zvc {
@@ -471,6 +473,55 @@ __global__ void __launch_bounds__(kMaxThreads)
   }
 }
 
+// Shared memory of a split-mode CTA whose buffer holds cap words.
+inline uint64_t split_smem_bytes(uint32_t cap, uint32_t wpc) {
+  return 4ull * round_up_u64(kCtlWords + (uint64_t)cap + 2ull * wpc, 4);
+}
+
+// Widens *cap to the largest buffer that keeps the CTAs per SM the launch needs: as many as
+// the mean-sized buffer allows, or fewer when fewer hold every chunk in as many waves (a
+// launch of one wave gains nothing from more). A larger buffer stages fewer chunks in
+// pieces. The device's SM count and shared memory are read once per device.
+template <int MAXT>
+zvc_status widen_cap(uint64_t chunks, uint32_t wpc, uint32_t full_cap, uint32_t* cap) {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> sms_of[kMaxDevices], smem_of[kMaxDevices], reserved_of[kMaxDevices];
+  cudaError_t e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_failure(e);
+  if (dev < 0 || dev >= kMaxDevices) return ZVC_ERR_INVALID_ARG;
+  int sms = sms_of[dev].load(), smem_sm = smem_of[dev].load(), reserved = reserved_of[dev].load();
+  if (sms == 0) {
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_failure(e);
+    smem_of[dev].store(smem_sm);
+    reserved_of[dev].store(reserved);
+    sms_of[dev].store(sms);
+  }
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decompress_kernel<MAXT>, 64,
+                                                    (size_t)split_smem_bytes(*cap, wpc));
+  if (e != cudaSuccess) return cuda_failure(e);
+  if (occ <= 0 || sms <= 0) return ZVC_OK;
+  const uint64_t waves = ceil_div_u64(chunks, (uint64_t)occ * sms);
+  const uint64_t need = ceil_div_u64(chunks, waves * sms);  // CTAs per SM, at most occ
+  const uint64_t per_cta = (uint64_t)smem_sm / need;
+  if (per_cta <= (uint64_t)reserved + 4ull * (kCtlWords + 2ull * wpc + 4)) return ZVC_OK;
+  uint64_t c = (per_cta - reserved) / 4 - kCtlWords - round_up_u64(2ull * wpc, 4);
+  c = (c & ~3ull) < full_cap ? (c & ~3ull) : (uint64_t)full_cap;
+  if (c <= *cap) return ZVC_OK;
+  int occ2 = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, decompress_kernel<MAXT>, 64,
+                                                    (size_t)split_smem_bytes((uint32_t)c, wpc));
+  if (e != cudaSuccess) return cuda_failure(e);
+  if ((uint64_t)occ2 >= need) *cap = (uint32_t)c;
+  return ZVC_OK;
+}
+
 template <int MAXT>
 zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, uint32_t T,
                     bool batched, uint32_t C, uint8_t* ws, cudaStream_t stream) {
@@ -496,28 +547,37 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   // the largest valid chunk (C/32 masks + C words) at any 16-byte phase
   const uint32_t full_cap = (uint32_t)round_up_u64(wpc + C + 3ull, 4);
   args.solo = C <= 2048 ? 1u : 0u;
-  args.cap_words = full_cap;
-  if (!args.solo && chunks > 0) {
-    // A CTA's shared memory is fixed at launch and sets how many chunks are in flight per
-    // SM, so the buffer is sized from the mean chunk length (the stream's size less its
-    // headers and tables): chunks up to kCapSlack times the mean go in one piece.
-    const uint64_t fixed = (batched ? 16ull + 8ull * ((uint64_t)T + 1) : 0ull) + 32ull * T +
-                           8ull * chunks;
-    const uint64_t mean = min((uint64_t)full_cap, in_bytes > fixed ? (in_bytes - fixed) / 4 / chunks : 0);
-    const uint64_t want = round_up_u64(mean * kCapSlackNum / kCapSlackDen + kCapExtraWords, 4);
-    args.cap_words = (uint32_t)min((uint64_t)full_cap, max((uint64_t)kCapMinWords, want));
-  }
-  args.meta_offset_words = args.cap_words;
-  args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.cap_words + 2ull * wpc, 4);
   args.chunks_per_cta = args.solo ? kSoloChunksPerCta : 1u;
   const uint32_t threads = args.solo ? 32u * kSoloChunksPerCta : 64u;
-  const uint64_t smem = 4ull * args.slot_words * args.chunks_per_cta;
-  cudaError_t e = cudaFuncSetAttribute(decompress_kernel<MAXT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the most shared memory a CTA of this chunk size can ask for, and all of the SM's
+  // unified memory as shared memory
+  cudaError_t e = cudaFuncSetAttribute(
+      decompress_kernel<MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)(split_smem_bytes(full_cap, wpc) * args.chunks_per_cta));
   if (e != cudaSuccess) return cuda_failure(e);
   e = cudaFuncSetAttribute(decompress_kernel<MAXT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            100);
   if (e != cudaSuccess) return cuda_failure(e);
+  args.cap_words = full_cap;
+  if (!args.solo && chunks > 0) {
+    // A CTA's shared memory is fixed at launch and sets how many chunks are in flight per
+    // SM, so the buffer is sized from the mean chunk length (the stream's size less its
+    // headers and tables): chunks up to 5/4 of the mean (+64 words) go in one piece. Then
+    // it is widened as far as the CTAs per SM the launch needs allow.
+    const uint64_t fixed = (batched ? 16ull + 8ull * ((uint64_t)T + 1) : 0ull) + 32ull * T +
+                           8ull * chunks;
+    const uint64_t mean =
+        min((uint64_t)full_cap, in_bytes > fixed ? (in_bytes - fixed) / 4 / chunks : 0);
+    const uint64_t want = round_up_u64(mean * kCapSlackNum / kCapSlackDen + kCapExtraWords, 4);
+    args.cap_words = (uint32_t)min((uint64_t)full_cap, max((uint64_t)kCapMinWords, want));
+    if (args.cap_words < full_cap) {
+      const zvc_status st = widen_cap<MAXT>(chunks, wpc, full_cap, &args.cap_words);
+      if (st != ZVC_OK) return st;
+    }
+  }
+  args.meta_offset_words = args.cap_words;
+  args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.cap_words + 2ull * wpc, 4);
+  const uint64_t smem = 4ull * args.slot_words * args.chunks_per_cta;
   const uint64_t blocks = ceil_div_u64(args.total_items, args.chunks_per_cta);
   const TraceMark mark = trace_begin(kTraceDecompress, stream);
   decompress_kernel<MAXT><<<(unsigned)blocks, threads, smem, stream>>>(args);
