@@ -92,11 +92,11 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
   return v;
 }
 
-// Warp 0: validate, stage and walk. Returns with ctl.state set to 1 (table complete and
-// checked) or 2 (give up; an error is latched unless the item had no chunk).
+// One thread per chunk: validate, stage and walk. Returns with ctl.state set to 1 (table
+// complete and checked) or 2 (give up; an error is latched unless the item had no chunk).
 template <int MAXT>
 __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32_t* dsm,
-                       Control* ec, uint64_t item, uint32_t lane) {
+                       Control* ec, uint64_t item) {
   const uint32_t C = a.chunk_elems;
   uint32_t* buf = dsm + kCtlWords;
   uint2* wmeta = reinterpret_cast<uint2*>(dsm + kCtlWords + a.meta_offset_words);
@@ -119,11 +119,11 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
   const uint64_t n = ti < a.T ? a.n[ti] : 0;
   const uint64_t nc = ceil_div_u64(n, C);
   auto give_up = [&](uint32_t code) {
-    if (code != 0 && lane == 0) latch_error(ec, code, item);
-    if (lane == 0) st_release_cta(&ctl.state, 2u);
+    if (code != 0) latch_error(ec, code, item);
+    st_release_cta(&ctl.state, 2u);
   };
 
-  // ---- locate and validate the stream (all lanes compute the same values). Every
+  // ---- locate and validate the stream. Every
   // address read here is in bounds by sizes known before the round's loads, so each
   // round issues all its loads at once: the batch table, then the stream header and the
   // chunk's table entries.
@@ -184,8 +184,8 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
   }
 
   // ---- stage the chunk: its words sit in shared memory at the same 16-byte phase as in
-  // global memory, so one bulk copy moves the aligned body; lanes load the at most three
-  // words on either side. The buffer holds cap words; a longer chunk is staged in pieces
+  // global memory, so one bulk copy moves the aligned body and plain loads the at most
+  // three words on either side. The buffer holds cap words; a longer chunk is staged in pieces
   // (below), the first piece being its first cap - phase words.
   const uint32_t len = (uint32_t)((end - start) / 4);
   const uint32_t* cw = sw + kStreamHeaderWords + 2 * nc + start / 4;
@@ -197,22 +197,27 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
     const uint32_t head = min(e, (4u - ph) & 3u);
     const uint32_t body = (e - head) & ~3u;
     const uint32_t tail = e - head - body;
-    if (body > 0 && lane == 0) {
+    uint32_t x[6];
+#pragma unroll
+    for (uint32_t i = 0; i < 3; ++i) {
+      x[i] = i < head ? __ldcs(cw + i) : 0u;
+      x[3 + i] = i < tail ? __ldcs(cw + head + body + i) : 0u;
+    }
+    if (body > 0) {
       mbar_arrive_expect_tx(&ctl.full, body * 4);
       bulk_g2s(buf + ph + head, cw + head, body * 4, &ctl.full);
     }
-    if (lane < head) buf[ph + lane] = __ldcs(cw + lane);
-    if (lane < tail) buf[ph + head + body + lane] = __ldcs(cw + head + body + lane);
-    __threadfence_block();  // the end words are published with the staged count
-    __syncwarp();
+#pragma unroll
+    for (uint32_t i = 0; i < 3; ++i) {
+      if (i < head) buf[ph + i] = x[i];
+      if (i < tail) buf[ph + head + body + i] = x[3 + i];
+    }
     if (body > 0 && !mbar_wait(&ctl.full, 0, a.wait_limit_ns)) {
       give_up(ZVC_ERR_TIMEOUT);
       return;
     }
     fills = body > 0 ? 1u : 0u;
-    __syncwarp();
   }
-  if (lane != 0) return;
   st_release_cta(&ctl.progress, 1u);  // staged: the scatterer may read the piece
 
   // ---- walk the masks. The chain position -> mask -> next position is the critical
@@ -435,6 +440,8 @@ constexpr uint32_t kSoloChunksPerCta = 8;
 // 1024 words (a piece then holds at least 31 windows).
 constexpr uint64_t kCapSlackNum = 5, kCapSlackDen = 4, kCapExtraWords = 64;
 constexpr uint32_t kCapMinWords = 1024;
+constexpr uint32_t kSplitMaxChunksPerCta = 4;  // chunks one walker warp walks at once
+constexpr uint64_t kMultiMeanDiv = 6;          // several chunks per CTA: mean <= largest / 6
 constexpr uint32_t kMaxThreads = 256;
 
 template <int MAXT>
@@ -442,18 +449,21 @@ __global__ void __launch_bounds__(kMaxThreads)
     decompress_kernel(const __grid_constant__ DecompressArgs<MAXT> a) {
   extern __shared__ __align__(16) uint32_t dsm_all[];
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-  const uint32_t k = a.solo ? warp : warp >> 1;  // this warp's chunk within the CTA
+  // this thread's chunk within the CTA: solo, warp k walks and scatters chunk k; split,
+  // lane k of warp 0 walks chunk k and warp k + 1 scatters it
+  const uint32_t k = a.solo ? warp : (warp == 0 ? min(lane, a.chunks_per_cta - 1) : warp - 1);
   uint32_t* dsm = dsm_all + (uint64_t)k * a.slot_words;
   DecompressCtl& ctl = *reinterpret_cast<DecompressCtl*>(dsm);
   const uint64_t item = (uint64_t)blockIdx.x * a.chunks_per_cta + k;
   Control* ec = reinterpret_cast<Control*>(a.ws);
-  if (lane == 0 && (a.solo || (warp & 1u) == 0)) {
-    mbar_init(&ctl.full, 1);
+  if (threadIdx.x < a.chunks_per_cta) {
+    DecompressCtl& c0 = *reinterpret_cast<DecompressCtl*>(dsm_all + (uint64_t)threadIdx.x * a.slot_words);
+    mbar_init(&c0.full, 1);
     fence_mbar_init();
-    ctl.progress = 0;
-    ctl.state = 0;
-    ctl.drain = 0;
-    ctl.expanded = 0;
+    c0.progress = 0;
+    c0.state = 0;
+    c0.drain = 0;
+    c0.expanded = 0;
   }
   // the window tables start cleared: an entry is taken once it reads non-zero
   for (uint32_t c2 = 0; c2 < a.chunks_per_cta; ++c2) {
@@ -461,14 +471,15 @@ __global__ void __launch_bounds__(kMaxThreads)
     for (uint32_t i = threadIdx.x; i < 2u * (a.chunk_elems / kWindow); i += blockDim.x) wz[i] = 0u;
   }
   __syncthreads();
-  if (item >= a.total_items) return;
   if (a.solo) {
-    walker(a, ctl, dsm, ec, item, lane);
+    if (item >= a.total_items) return;
+    if (lane == 0) walker(a, ctl, dsm, ec, item);
     __syncwarp();
     scatterer(a, ctl, dsm, ec, item, lane);
-  } else if ((warp & 1u) == 0) {
-    walker(a, ctl, dsm, ec, item, lane);
+  } else if (warp == 0) {
+    if (lane < a.chunks_per_cta && item < a.total_items) walker(a, ctl, dsm, ec, item);
   } else {
+    if (item >= a.total_items) return;
     scatterer(a, ctl, dsm, ec, item, lane);
   }
 }
@@ -478,47 +489,91 @@ inline uint64_t split_smem_bytes(uint32_t cap, uint32_t wpc) {
   return 4ull * round_up_u64(kCtlWords + (uint64_t)cap + 2ull * wpc, 4);
 }
 
-// Widens *cap to the largest buffer that keeps the CTAs per SM the launch needs: as many as
-// the mean-sized buffer allows, or fewer when fewer hold every chunk in as many waves (a
-// launch of one wave gains nothing from more). A larger buffer stages fewer chunks in
-// pieces. The device's SM count and shared memory are read once per device.
-template <int MAXT>
-zvc_status widen_cap(uint64_t chunks, uint32_t wpc, uint32_t full_cap, uint32_t* cap) {
+struct DeviceLimits {
+  int sms, smem_per_sm, reserved_per_cta, smem_per_cta_max;
+};
+
+// The device's SM count and shared memory, read once per device.
+zvc_status device_limits(DeviceLimits* d) {
   constexpr int kMaxDevices = 64;
-  static std::atomic<int> sms_of[kMaxDevices], smem_of[kMaxDevices], reserved_of[kMaxDevices];
+  static std::atomic<int> sms_of[kMaxDevices], smem_of[kMaxDevices], reserved_of[kMaxDevices],
+      cta_max_of[kMaxDevices];
   cudaError_t e;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_failure(e);
   if (dev < 0 || dev >= kMaxDevices) return ZVC_ERR_INVALID_ARG;
-  int sms = sms_of[dev].load(), smem_sm = smem_of[dev].load(), reserved = reserved_of[dev].load();
-  if (sms == 0) {
-    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
-            cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
-            cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+  d->sms = sms_of[dev].load();
+  d->smem_per_sm = smem_of[dev].load();
+  d->reserved_per_cta = reserved_of[dev].load();
+  d->smem_per_cta_max = cta_max_of[dev].load();
+  if (d->sms == 0) {
+    if ((e = cudaDeviceGetAttribute(&d->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                    dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d->reserved_per_cta, cudaDevAttrReservedSharedMemoryPerBlock,
+                                    dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d->smem_per_cta_max, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                    dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_failure(e);
-    smem_of[dev].store(smem_sm);
-    reserved_of[dev].store(reserved);
-    sms_of[dev].store(sms);
+    smem_of[dev].store(d->smem_per_sm);
+    reserved_of[dev].store(d->reserved_per_cta);
+    cta_max_of[dev].store(d->smem_per_cta_max);
+    sms_of[dev].store(d->sms);
   }
+  return ZVC_OK;
+}
+
+// CTAs of k chunks with buffers of cap words that fit on one SM.
+template <int MAXT>
+zvc_status split_occupancy(uint32_t k, uint32_t cap, uint32_t wpc, int* occ) {
+  *occ = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      occ, decompress_kernel<MAXT>, (int)(32 * (1 + k)), (size_t)(k * split_smem_bytes(cap, wpc)));
+  return e == cudaSuccess ? ZVC_OK : cuda_failure(e);
+}
+
+// Split mode: with short chunks (a mean of at most 1/6 of the largest) in a launch of two
+// waves or more, the chunks per CTA (1, 2 or 4; one walker warp walks them all, one lane
+// each) that keep the most chunks in flight per SM, preferring more per CTA on a tie: the
+// kernel is then bound by the instructions it issues, and a shared walker warp issues a
+// quarter of them per chunk. Otherwise one chunk per CTA: a CTA frees its shared memory
+// only when its slowest chunk is done. Then widens *cap to the largest buffer that keeps
+// the CTAs per SM the launch needs: as many as fit, or fewer when fewer hold every chunk in
+// as many waves. A larger buffer stages fewer chunks in pieces.
+template <int MAXT>
+zvc_status plan_split(const DeviceLimits& d, uint64_t chunks, uint64_t mean, uint32_t wpc,
+                      uint32_t full_cap, uint32_t* cap, uint32_t* chunks_per_cta) {
+  zvc_status st;
+  uint32_t k = 1;
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decompress_kernel<MAXT>, 64,
-                                                    (size_t)split_smem_bytes(*cap, wpc));
-  if (e != cudaSuccess) return cuda_failure(e);
-  if (occ <= 0 || sms <= 0) return ZVC_OK;
-  const uint64_t waves = ceil_div_u64(chunks, (uint64_t)occ * sms);
-  const uint64_t need = ceil_div_u64(chunks, waves * sms);  // CTAs per SM, at most occ
-  const uint64_t per_cta = (uint64_t)smem_sm / need;
-  if (per_cta <= (uint64_t)reserved + 4ull * (kCtlWords + 2ull * wpc + 4)) return ZVC_OK;
-  uint64_t c = (per_cta - reserved) / 4 - kCtlWords - round_up_u64(2ull * wpc, 4);
-  c = (c & ~3ull) < full_cap ? (c & ~3ull) : (uint64_t)full_cap;
+  if ((st = split_occupancy<MAXT>(1, *cap, wpc, &occ)) != ZVC_OK) return st;
+  const bool short_chunks = mean * kMultiMeanDiv <= full_cap;
+  const bool waves2 = occ > 0 && chunks >= 2ull * (uint64_t)occ * d.sms;
+  uint64_t best = (uint64_t)occ;
+  for (uint32_t kk = 2; short_chunks && waves2 && kk <= kSplitMaxChunksPerCta; kk *= 2) {
+    if (kk * split_smem_bytes(*cap, wpc) > (uint64_t)d.smem_per_cta_max) break;
+    int o = 0;
+    if ((st = split_occupancy<MAXT>(kk, *cap, wpc, &o)) != ZVC_OK) return st;
+    if ((uint64_t)o * kk >= best && o > 0) {
+      best = (uint64_t)o * kk;
+      k = kk;
+      occ = o;
+    }
+  }
+  *chunks_per_cta = k;
+  if (occ <= 0 || d.sms <= 0 || *cap >= full_cap) return ZVC_OK;
+  const uint64_t ctas = ceil_div_u64(chunks, k);
+  const uint64_t waves = ceil_div_u64(ctas, (uint64_t)occ * d.sms);
+  const uint64_t need = ceil_div_u64(ctas, waves * d.sms);  // CTAs per SM, at most occ
+  const uint64_t per_cta = min((uint64_t)d.smem_per_sm / need, (uint64_t)d.smem_per_cta_max + d.reserved_per_cta);
+  const uint64_t fixed = (uint64_t)d.reserved_per_cta + 4ull * k * (kCtlWords + round_up_u64(2ull * wpc, 4));
+  if (per_cta <= fixed + 16ull * k) return ZVC_OK;
+  uint64_t c = ((per_cta - fixed) / (4ull * k)) & ~3ull;
+  c = c < full_cap ? c : (uint64_t)full_cap;
   if (c <= *cap) return ZVC_OK;
-  int occ2 = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, decompress_kernel<MAXT>, 64,
-                                                    (size_t)split_smem_bytes((uint32_t)c, wpc));
-  if (e != cudaSuccess) return cuda_failure(e);
-  if ((uint64_t)occ2 >= need) *cap = (uint32_t)c;
+  int o2 = 0;
+  if ((st = split_occupancy<MAXT>(k, (uint32_t)c, wpc, &o2)) != ZVC_OK) return st;
+  if ((uint64_t)o2 >= need) *cap = (uint32_t)c;
   return ZVC_OK;
 }
 
@@ -548,12 +603,16 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   const uint32_t full_cap = (uint32_t)round_up_u64(wpc + C + 3ull, 4);
   args.solo = C <= 2048 ? 1u : 0u;
   args.chunks_per_cta = args.solo ? kSoloChunksPerCta : 1u;
-  const uint32_t threads = args.solo ? 32u * kSoloChunksPerCta : 64u;
-  // the most shared memory a CTA of this chunk size can ask for, and all of the SM's
-  // unified memory as shared memory
+  DeviceLimits d;
+  zvc_status st = device_limits(&d);
+  if (st != ZVC_OK) return st;
+  // the most shared memory a CTA of this chunk size can ask for (within the device's
+  // limit), and all of the SM's unified memory as shared memory
+  const uint64_t most = split_smem_bytes(full_cap, wpc) *
+                        (args.solo ? kSoloChunksPerCta : kSplitMaxChunksPerCta);
   cudaError_t e = cudaFuncSetAttribute(
       decompress_kernel<MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)(split_smem_bytes(full_cap, wpc) * args.chunks_per_cta));
+      (int)min(most, (uint64_t)d.smem_per_cta_max));
   if (e != cudaSuccess) return cuda_failure(e);
   e = cudaFuncSetAttribute(decompress_kernel<MAXT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            100);
@@ -570,14 +629,13 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
         min((uint64_t)full_cap, in_bytes > fixed ? (in_bytes - fixed) / 4 / chunks : 0);
     const uint64_t want = round_up_u64(mean * kCapSlackNum / kCapSlackDen + kCapExtraWords, 4);
     args.cap_words = (uint32_t)min((uint64_t)full_cap, max((uint64_t)kCapMinWords, want));
-    if (args.cap_words < full_cap) {
-      const zvc_status st = widen_cap<MAXT>(chunks, wpc, full_cap, &args.cap_words);
-      if (st != ZVC_OK) return st;
-    }
+    st = plan_split<MAXT>(d, chunks, mean, wpc, full_cap, &args.cap_words, &args.chunks_per_cta);
+    if (st != ZVC_OK) return st;
   }
   args.meta_offset_words = args.cap_words;
   args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.cap_words + 2ull * wpc, 4);
   const uint64_t smem = 4ull * args.slot_words * args.chunks_per_cta;
+  const uint32_t threads = args.solo ? 32u * kSoloChunksPerCta : 32u * (1u + args.chunks_per_cta);
   const uint64_t blocks = ceil_div_u64(args.total_items, args.chunks_per_cta);
   const TraceMark mark = trace_begin(kTraceDecompress, stream);
   decompress_kernel<MAXT><<<(unsigned)blocks, threads, smem, stream>>>(args);

@@ -83,6 +83,32 @@ def test_corrupt_chunks_staged_in_pieces_agree_with_oracle():
     assert seen[zvc.ZVC_ERR_CORRUPT] > 20 and seen[zvc.ZVC_OK] > 5, seen
 
 
+def test_corrupt_short_chunks_agree_with_oracle():
+    """Flipped bits in a stream of 8192 sparse chunks, decompressed by CTAs that hold several
+    chunks each (one warp walking them all): status and words must be the oracle's."""
+    ensure_lib()
+    rng = np.random.default_rng(26)
+    C = 4096
+    n = 8192 * C
+    w = _rand(rng, n, 0.03)
+    s = oracle.encode(w, C)
+    table_end = 32 + 8 * (n // C)
+    seen = {zvc.ZVC_OK: 0, zvc.ZVC_ERR_CORRUPT: 0}
+    for trial in range(8):
+        t = s.copy()
+        for _ in range(int(rng.integers(1, 4))):
+            i = int(rng.integers(table_end, t.size))
+            t[i] ^= np.uint8(1 << int(rng.integers(0, 8)))
+        ost, owords = oracle.decode(t, n, C)
+        gst, gwords = _gpu_status(t, n, C)
+        if ost == oracle.OK:
+            assert gst == zvc.ZVC_OK and np.array_equal(gwords, owords), trial
+        else:
+            assert gst == zvc.ZVC_ERR_CORRUPT, (trial, ost, gst)
+        seen[gst] += 1
+    assert seen[zvc.ZVC_ERR_CORRUPT] >= 3, seen
+
+
 def test_size_and_parameter_mismatches():
     rng = np.random.default_rng(22)
     w = _rand(rng, 50_000, 0.4)

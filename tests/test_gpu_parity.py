@@ -131,6 +131,18 @@ def test_chunks_longer_than_the_mean_unaligned(off):
     assert np.array_equal(out.cpu().numpy().view(np.uint32), w)
 
 
+@pytest.mark.parametrize("cut", [0, 4096 * 3 + 101])
+def test_many_short_chunks(cut):
+    """8192 sparse chunks (3% non-zero): a launch of more than two waves of short chunks,
+    where a decompressing CTA holds several chunks and one warp walks them all."""
+    rng = np.random.default_rng(40 + cut)
+    w = _random_words(rng, 8192 * 4096 - cut, 0.03)
+    w[: 4096 * 2] = _random_words(rng, 4096 * 2, 1.0)  # two dense chunks among them
+    st, err, back = gpu_decompress(oracle.encode(w, 4096), w.size, 4096)
+    assert st == zvc.ZVC_OK and err == zvc.ZVC_OK
+    assert np.array_equal(back, w)
+
+
 def test_single_relu_config_bit_exact():
     x = workloads.single_relu(device="cuda")[0]
     w = words_of(x)
