@@ -3,20 +3,23 @@
 // section V.B has the engine expand compressed data into 128-byte lines using the masks'
 // prefix counts as scatter offsets).
 //
-// A chunk, located through the stream's chunk offset table, is decoded by a walker and a
-// scatterer: two warps of a CTA of its own (chunks over 2048 words), or one warp that
-// walks and then scatters (smaller chunks, 8 per CTA). The walker:
+// A chunk, located through the stream's chunk offset table, is decoded by a walker (one
+// thread) and a scatterer (one warp). Chunks over 2048 words: a CTA holds k chunks (k = 1,
+// or 2 or 4 for short chunks), lane i of warp 0 walks chunk i and warp i + 1 scatters it.
+// Smaller chunks: 8 per CTA, one warp each, whose lane 0 walks before the warp scatters.
+// The walker:
 //   validate  batch table (if any), stream header and this chunk's table entries; every
 //             check that fails latches ZVC_ERR_CORRUPT before any access to the chunk
 //   stage     the chunk's compressed words are copied into shared memory by a 1-D TMA
-//             bulk copy (plain loads for the unaligned ends), at their 16-byte phase
-//   walk      a window's position depends on every earlier mask, so one lane walks the
+//             bulk copy (plain loads for the unaligned ends), at their 16-byte phase; the
+//             buffer is sized on the host from the stream's mean chunk, and a longer
+//             chunk goes in pieces, each started once the scatterer has drained the last
+//   walk      a window's position depends on every earlier mask, so one thread walks the
 //             masks (position += 1 + popc(mask)), recording each window's (first value,
 //             mask) in one 8-byte store into a table that starts cleared; the walk must
 //             end exactly at the next chunk's offset
-// The scatterer expands windows as soon as it reads their entries non-zero, so with two
-// warps the
-// scatter runs under the walk: lane l expands words 4(l mod 8) .. +3 of window l/8 + 4k of each
+// The scatterer expands windows as soon as it reads their entries non-zero, so the scatter
+// runs under the walk: lane l expands words 4(l mod 8) .. +3 of window l/8 + 4k of each
 // group of 16 windows, a set bit at position b reading packed word popc(mask & (2^b - 1)),
 // a clear bit writing 0, with 16-byte stores.
 // Extra work items (one per tensor, after the chunks) check the headers of streams that
@@ -28,8 +31,9 @@
 namespace zvc {
 namespace {
 
-// Shared memory of a CTA: control words, then the chunk buffer (C/32 masks + C words, +3
-// for the 16-byte phase), then the window table (first value, mask) per window.
+// Shared memory of a chunk's slot: control words, then the chunk buffer (cap words, at
+// most C/32 masks + C words + 3 for the 16-byte phase), then the window table (first
+// value, mask) per window. A CTA holds chunks_per_cta slots.
 struct DecompressCtl {
   uint64_t full;      // mbarrier of the TMA copies, one phase per bulk copy
   uint32_t progress;  // pieces of the chunk staged so far
@@ -433,8 +437,8 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
 }
 
 // A chunk of up to 2048 words walks in at most 64 steps, so one warp walks it and then
-// expands it, and 8 chunks share a CTA; a larger chunk gets a walker and a scatterer warp
-// and a CTA of its own.
+// expands it, and 8 chunks share a CTA; a larger chunk gets a scatterer warp of its own,
+// and a lane of the CTA's walker warp (the host picks the chunks per CTA).
 constexpr uint32_t kSoloChunksPerCta = 8;
 // Buffer of a CTA with a chunk over 2048 words: 5/4 of the mean chunk + 64 words, at least
 // 1024 words (a piece then holds at least 31 windows).
