@@ -248,6 +248,16 @@ __device__ __forceinline__ uint32_t pack_window(uint32_t* slot, uint32_t pos, ui
   return pos + 1u + __popc(m);
 }
 
+// The same with the position as a byte offset into the slot, which saves the scaling of
+// both store addresses.
+__device__ __forceinline__ uint32_t pack_window_bytes(char* slot, uint32_t pb, uint32_t v,
+                                                      uint32_t m, uint32_t lane,
+                                                      uint32_t lane_below) {
+  if (v != 0u) *reinterpret_cast<uint32_t*>(slot + pb + 4u * __popc(m & lane_below) + 4u) = v;
+  if (lane == 0) *reinterpret_cast<uint32_t*>(slot + pb) = m;
+  return pb + 4u * __popc(m) + 4u;
+}
+
 template <int MAXT>
 __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint64_t* status,
                           Control* ctl, uint32_t team, uint32_t q, uint32_t lane) {
@@ -283,14 +293,18 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
         v[j] = e < valid ? __ldcs(src + e) : 0u;
       }
     }
-    // masks and the warp's payload words
+    // masks and the warp's payload words: a mask per window it holds (the windows past a
+    // ragged tile's end hold only zeros, so they add no words) and every non-zero word,
+    // counted per lane and summed over the warp
     uint32_t m[kWinPerWarp];
-    uint32_t tot = 0;
+    uint32_t nz = 0;
 #pragma unroll
     for (uint32_t j = 0; j < kWinPerWarp; ++j) {
       m[j] = __ballot_sync(0xffffffffu, v[j] != 0u);
-      tot += w0 + j < nwin ? 1u + __popc(m[j]) : 0u;
+      nz += v[j] != 0u ? 1u : 0u;
     }
+    const uint32_t held = nwin > w0 ? min(nwin - w0, kWinPerWarp) : 0u;
+    const uint32_t tot = held + __reduce_add_sync(0xffffffffu, nz);
     uint32_t* tt = sm.team_tot[team][round & 1u];
     if (lane == 0) tt[q] = tot;
     team_sync(team);  // every word of the tile is read and every warp total is in
@@ -307,8 +321,11 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
     // (by lane 0), which costs fewer instructions than folding the mask into the lanes
     // holding a zero and testing every window for having none
     if (nwin == kTileWindows && !keep_woff) {
+      char* sb = reinterpret_cast<char*>(slot);
+      uint32_t pb = 4u * pos;
 #pragma unroll
-      for (uint32_t j = 0; j < kWinPerWarp; ++j) pos = pack_window(slot, pos, v[j], m[j], lane, lane_below);
+      for (uint32_t j = 0; j < kWinPerWarp; ++j)
+        pb = pack_window_bytes(sb, pb, v[j], m[j], lane, lane_below);
     } else {  // chunks start inside tiles (their windows' offsets are kept), or ragged tile
 #pragma unroll
       for (uint32_t j = 0; j < kWinPerWarp; ++j) {
