@@ -235,10 +235,6 @@ __device__ __forceinline__ bool team_any(uint32_t team, bool c) {
   return r != 0;
 }
 
-__device__ __forceinline__ void team_sync(uint32_t team) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1u + team), "n"(kTeamWarps * 32) : "memory");
-}
-
 // Writes one window (this lane's word v, the window's mask m) at word pos of the slot and
 // returns the position after it.
 __device__ __forceinline__ uint32_t pack_window(uint32_t* slot, uint32_t pos, uint32_t v,
@@ -270,17 +266,17 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
     const unsigned long long t = blockIdx.x + (unsigned long long)i * G;
     if (t >= a.total_tiles) return;
     const int s = (int)(i % kSlots);
+    // a warp whose wait ran out reads nothing; the team learns of it at its barrier below
     const bool late = !mbar_wait(&sm.full[s], (i / kSlots) & 1u, a.wait_limit_ns);
-    if (team_any(team, late)) {
-      if (q == 0 && lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
-      return;
-    }
     const SlotInfo& f = sm.info[s];
     uint32_t* slot = sm.slot[s];
     // read: this lane's word of each of the warp's 16 windows
     uint32_t v[kWinPerWarp];
     uint32_t nwin = kTileWindows;
-    if (!f.direct) {
+    if (late) {
+#pragma unroll
+      for (uint32_t j = 0; j < kWinPerWarp; ++j) v[j] = 0u;
+    } else if (!f.direct) {
 #pragma unroll
       for (uint32_t j = 0; j < kWinPerWarp; ++j) v[j] = slot[kInOffset + (w0 + j) * kWindow + lane];
     } else {  // read from global memory; a ragged tile has fewer windows
@@ -307,7 +303,12 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
     const uint32_t tot = held + __reduce_add_sync(0xffffffffu, nz);
     uint32_t* tt = sm.team_tot[team][round & 1u];
     if (lane == 0) tt[q] = tot;
-    team_sync(team);  // every word of the tile is read and every warp total is in
+    // every word of the tile is read and every warp total is in; a late warp gives up the
+    // team's tile here, all its warps together
+    if (team_any(team, late)) {
+      if (q == 0 && lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
+      return;
+    }
     // lane r < kTeamWarps reads warp r's total: the warp's base and the tile's aggregate
     const uint32_t x = lane < kTeamWarps ? tt[lane] : 0u;
     const uint32_t pos0 = __reduce_add_sync(0xffffffffu, lane < q ? x : 0u);
