@@ -327,7 +327,15 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
 #pragma unroll
       for (uint32_t j = 0; j < kWinPerWarp; ++j)
         pb = pack_window_bytes(sb, pb, v[j], m[j], lane, lane_below);
-    } else {  // chunks start inside tiles (their windows' offsets are kept), or ragged tile
+    } else if (nwin == kTileWindows) {  // chunks start inside tiles: window offsets are kept
+      char* sb = reinterpret_cast<char*>(slot);
+      uint32_t pb = 4u * pos;
+#pragma unroll
+      for (uint32_t j = 0; j < kWinPerWarp; ++j) {
+        if (lane == 0) sm.woff[s][w0 + j] = pb >> 2;
+        pb = pack_window_bytes(sb, pb, v[j], m[j], lane, lane_below);
+      }
+    } else {  // a ragged tile
 #pragma unroll
       for (uint32_t j = 0; j < kWinPerWarp; ++j) {
         if (w0 + j < nwin) {
@@ -477,12 +485,12 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
       if (!a.inner_chunks) {  // chunks are whole tiles: at most window 0 starts one
         if (lane == 0 && w_first % wpc == 0)
           put_u64_words(table + 2 * (w_first / wpc), 4 * in_stream);
-      } else {
+      } else {  // the first chunk starting in the tile, then one every wpc windows
         const uint32_t nwin = (f.valid + kWindow - 1) / kWindow;
-        for (uint32_t w = lane; w < nwin; w += 32) {
-          const uint64_t wg = w_first + w;
-          if (wg % wpc == 0) put_u64_words(table + 2 * (wg / wpc), 4 * (in_stream + sm.woff[s][w]));
-        }
+        const uint64_t c0 = (w_first + wpc - 1) / wpc;
+        const uint32_t first = (uint32_t)(c0 * wpc - w_first);
+        for (uint32_t w = first + lane * wpc, c = lane; w < nwin; w += 32 * wpc, c += 32)
+          put_u64_words(table + 2 * (c0 + c), 4 * (in_stream + sm.woff[s][w]));
       }
     }
     // the slot is read; it takes tile i + kSlots next
