@@ -4,9 +4,8 @@
 // prefix counts as scatter offsets).
 //
 // A chunk, located through the stream's chunk offset table, is decoded by a walker (one
-// thread) and a scatterer (one warp). Chunks over 2048 words: a CTA holds k chunks (k = 1,
-// or 2 or 4 for short chunks), lane i of warp 0 walks chunk i and warp i + 1 scatters it.
-// Smaller chunks: 8 per CTA, one warp each, whose lane 0 walks before the warp scatters.
+// thread) and a scatterer (one warp). A CTA holds k chunks (k = 1, or 2 or 4 for short
+// chunks): lane i of warp 0 walks chunk i and warp i + 1 scatters it.
 // The walker:
 //   validate  batch table (if any), stream header and this chunk's table entries; every
 //             check that fails latches ZVC_ERR_CORRUPT before any access to the chunk
@@ -75,7 +74,6 @@ struct DecompressArgs {
   uint32_t cap_words;          // chunk buffer words (a multiple of 4): longer chunks go in pieces
   uint32_t meta_offset_words;  // window table, 8-byte aligned
   uint32_t chunks_per_cta;
-  uint32_t solo;               // 1: one warp walks and then scatters its chunk
   uint32_t slot_words;         // shared memory of one chunk: control, buffer, table
   uint32_t* out[MAXT];
   uint64_t n[MAXT];
@@ -265,7 +263,7 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
     }
     // the window runs past the buffer: past the chunk in its last piece (corrupt), else
     // the next piece starts at this window
-    if (e >= len || a.solo) {
+    if (e >= len) {
       good = false;
       break;
     }
@@ -436,26 +434,24 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
   }
 }
 
-// A chunk of up to 2048 words walks in at most 64 steps, so one warp walks it and then
-// expands it, and 8 chunks share a CTA; a larger chunk gets a scatterer warp of its own,
-// and a lane of the CTA's walker warp (the host picks the chunks per CTA).
-constexpr uint32_t kSoloChunksPerCta = 8;
-// Buffer of a CTA with a chunk over 2048 words: 5/4 of the mean chunk + 64 words, at least
-// 1024 words (a piece then holds at least 31 windows).
+// Every chunk gets a scatterer warp of its own and a lane of the CTA's walker warp; the
+// host picks the chunks per CTA. A chunk's buffer: 5/4 of the mean chunk + 64 words, at
+// least 1024 words (a piece then holds at least 31 windows), at most the largest chunk.
 constexpr uint64_t kCapSlackNum = 5, kCapSlackDen = 4, kCapExtraWords = 64;
 constexpr uint32_t kCapMinWords = 1024;
 constexpr uint32_t kSplitMaxChunksPerCta = 4;  // chunks one walker warp walks at once
-constexpr uint64_t kMultiMeanDiv = 6;          // several chunks per CTA: mean <= largest / 6
-constexpr uint32_t kMaxThreads = 256;
+constexpr uint64_t kMultiMeanDiv = 6;          // several chunks per CTA: mean <= largest / 6,
+constexpr uint32_t kMultiAnyWords = 1060;      // or chunks of at most 1024 elements
+constexpr uint32_t kMaxThreads = 32 * (1 + kSplitMaxChunksPerCta);
 
 template <int MAXT>
 __global__ void __launch_bounds__(kMaxThreads)
     decompress_kernel(const __grid_constant__ DecompressArgs<MAXT> a) {
   extern __shared__ __align__(16) uint32_t dsm_all[];
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-  // this thread's chunk within the CTA: solo, warp k walks and scatters chunk k; split,
-  // lane k of warp 0 walks chunk k and warp k + 1 scatters it
-  const uint32_t k = a.solo ? warp : (warp == 0 ? min(lane, a.chunks_per_cta - 1) : warp - 1);
+  // this thread's chunk within the CTA: lane k of warp 0 walks chunk k, warp k + 1
+  // scatters it
+  const uint32_t k = warp == 0 ? min(lane, a.chunks_per_cta - 1) : warp - 1;
   uint32_t* dsm = dsm_all + (uint64_t)k * a.slot_words;
   DecompressCtl& ctl = *reinterpret_cast<DecompressCtl*>(dsm);
   const uint64_t item = (uint64_t)blockIdx.x * a.chunks_per_cta + k;
@@ -475,12 +471,7 @@ __global__ void __launch_bounds__(kMaxThreads)
     for (uint32_t i = threadIdx.x; i < 2u * (a.chunk_elems / kWindow); i += blockDim.x) wz[i] = 0u;
   }
   __syncthreads();
-  if (a.solo) {
-    if (item >= a.total_items) return;
-    if (lane == 0) walker(a, ctl, dsm, ec, item);
-    __syncwarp();
-    scatterer(a, ctl, dsm, ec, item, lane);
-  } else if (warp == 0) {
+  if (warp == 0) {
     if (lane < a.chunks_per_cta && item < a.total_items) walker(a, ctl, dsm, ec, item);
   } else {
     if (item >= a.total_items) return;
@@ -488,7 +479,7 @@ __global__ void __launch_bounds__(kMaxThreads)
   }
 }
 
-// Shared memory of a split-mode CTA whose buffer holds cap words.
+// Shared memory of a chunk whose buffer holds cap words.
 inline uint64_t split_smem_bytes(uint32_t cap, uint32_t wpc) {
   return 4ull * round_up_u64(kCtlWords + (uint64_t)cap + 2ull * wpc, 4);
 }
@@ -536,8 +527,8 @@ zvc_status split_occupancy(uint32_t k, uint32_t cap, uint32_t wpc, int* occ) {
   return e == cudaSuccess ? ZVC_OK : cuda_failure(e);
 }
 
-// Split mode: with short chunks (a mean of at most 1/6 of the largest) in a launch of two
-// waves or more, the chunks per CTA (1, 2 or 4; one walker warp walks them all, one lane
+// With short chunks (a mean of at most 1/6 of the largest, or chunks of at most 1024
+// elements) in a launch of two waves or more, the chunks per CTA (1, 2 or 4; one walker warp walks them all, one lane
 // each) that keep the most chunks in flight per SM, preferring more per CTA on a tie: the
 // kernel is then bound by the instructions it issues, and a shared walker warp issues a
 // quarter of them per chunk. Otherwise one chunk per CTA: a CTA frees its shared memory
@@ -551,7 +542,7 @@ zvc_status plan_split(const DeviceLimits& d, uint64_t chunks, uint64_t mean, uin
   uint32_t k = 1;
   int occ = 0;
   if ((st = split_occupancy<MAXT>(1, *cap, wpc, &occ)) != ZVC_OK) return st;
-  const bool short_chunks = mean * kMultiMeanDiv <= full_cap;
+  const bool short_chunks = mean * kMultiMeanDiv <= full_cap || full_cap <= kMultiAnyWords;
   const bool waves2 = occ > 0 && chunks >= 2ull * (uint64_t)occ * d.sms;
   uint64_t best = (uint64_t)occ;
   for (uint32_t kk = 2; short_chunks && waves2 && kk <= kSplitMaxChunksPerCta; kk *= 2) {
@@ -605,15 +596,13 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   const uint32_t wpc = C / kWindow;
   // the largest valid chunk (C/32 masks + C words) at any 16-byte phase
   const uint32_t full_cap = (uint32_t)round_up_u64(wpc + C + 3ull, 4);
-  args.solo = C <= 2048 ? 1u : 0u;
-  args.chunks_per_cta = args.solo ? kSoloChunksPerCta : 1u;
+  args.chunks_per_cta = 1u;
   DeviceLimits d;
   zvc_status st = device_limits(&d);
   if (st != ZVC_OK) return st;
   // the most shared memory a CTA of this chunk size can ask for (within the device's
   // limit), and all of the SM's unified memory as shared memory
-  const uint64_t most = split_smem_bytes(full_cap, wpc) *
-                        (args.solo ? kSoloChunksPerCta : kSplitMaxChunksPerCta);
+  const uint64_t most = split_smem_bytes(full_cap, wpc) * kSplitMaxChunksPerCta;
   cudaError_t e = cudaFuncSetAttribute(
       decompress_kernel<MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)min(most, (uint64_t)d.smem_per_cta_max));
@@ -622,7 +611,7 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
                            100);
   if (e != cudaSuccess) return cuda_failure(e);
   args.cap_words = full_cap;
-  if (!args.solo && chunks > 0) {
+  if (chunks > 0) {
     // A CTA's shared memory is fixed at launch and sets how many chunks are in flight per
     // SM, so the buffer is sized from the mean chunk length (the stream's size less its
     // headers and tables): chunks up to 5/4 of the mean (+64 words) go in one piece. Then
@@ -639,7 +628,7 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   args.meta_offset_words = args.cap_words;
   args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.cap_words + 2ull * wpc, 4);
   const uint64_t smem = 4ull * args.slot_words * args.chunks_per_cta;
-  const uint32_t threads = args.solo ? 32u * kSoloChunksPerCta : 32u * (1u + args.chunks_per_cta);
+  const uint32_t threads = 32u * (1u + args.chunks_per_cta);
   const uint64_t blocks = ceil_div_u64(args.total_items, args.chunks_per_cta);
   const TraceMark mark = trace_begin(kTraceDecompress, stream);
   decompress_kernel<MAXT><<<(unsigned)blocks, threads, smem, stream>>>(args);
