@@ -197,6 +197,25 @@ def _gpu_decompress_batched(stream, ns, C):
     return st, err, [o.cpu().numpy().view(np.uint32)[:n] for o, n in zip(outs, ns)]
 
 
+@pytest.mark.parametrize("C", [1024, 4096])
+def test_batched_many_short_chunks_with_empty_tensors(C):
+    """A batch of sparse tensors with empty ones among them, large enough that a
+    decompressing CTA holds several chunks: the header checks of the empty tensors run in
+    lanes of a walker warp that also walks chunks."""
+    rng = np.random.default_rng(50 + C)
+    ns = [(12000 if C == 1024 else 8000) * C + 77, 0, 1000, 0, 3 * C, 5 * C + 1]  # > 2 waves
+    ws_ = [_random_words(rng, n, 0.03) for n in ns]
+    ws_[4][: C] = _random_words(rng, C, 1.0)  # a dense chunk staged in pieces
+    ref = oracle.encode_batch(ws_, C)
+    st, err, backs = _gpu_decompress_batched(ref, ns, C)
+    assert st == zvc.ZVC_OK and err == zvc.ZVC_OK
+    for w, b in zip(ws_, backs):
+        assert np.array_equal(b, w)
+    got = _gpu_compress_batched([_dev_words(w) if w.size else
+                                 torch.empty(0, dtype=torch.int32, device="cuda") for w in ws_], C)
+    assert np.array_equal(got, ref)
+
+
 @pytest.mark.parametrize("name", golden_io.all_batch())
 def test_golden_batch(name):
     g = golden_io.load(name)
