@@ -41,7 +41,7 @@ struct DecompressCtl {
   uint32_t expanded;  // the windows before it are read out of the buffer (scatterer -> walker)
   uint32_t pad[2];
 };
-constexpr uint32_t kCtlWords = 8;       // sizeof(DecompressCtl) / 4, keeps the buffer 16-byte aligned
+constexpr uint32_t kCtlWords = 8;  // sizeof(DecompressCtl) / 4: the buffer stays 16-byte aligned
 static_assert(sizeof(DecompressCtl) == 4 * kCtlWords, "control words");
 constexpr uint32_t kPublishEvery = 16;  // the scatterer expands 16 windows at a time
 constexpr uint32_t kPollSleepNs = 32;   // the scatterer's sleep between polls of the table
@@ -369,7 +369,8 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
     }
     if (!waited(0)) return;
   }
-  const volatile unsigned long long* wm = reinterpret_cast<const volatile unsigned long long*>(wmeta);
+  const volatile unsigned long long* wm =
+      reinterpret_cast<const volatile unsigned long long*>(wmeta);
   const volatile uint32_t* drain = &ctl.drain;
   uint32_t g0 = 0, handled = 0;
   while (g0 < nwin) {
@@ -462,7 +463,8 @@ __global__ void __launch_bounds__(kMaxThreads, SMALL ? kSmallMinCtas : 0)
   const uint64_t item = (uint64_t)blockIdx.x * a.chunks_per_cta + k;
   Control* ec = reinterpret_cast<Control*>(a.ws);
   if (threadIdx.x < a.chunks_per_cta) {
-    DecompressCtl& c0 = *reinterpret_cast<DecompressCtl*>(dsm_all + (uint64_t)threadIdx.x * a.slot_words);
+    DecompressCtl& c0 =
+        *reinterpret_cast<DecompressCtl*>(dsm_all + (uint64_t)threadIdx.x * a.slot_words);
     mbar_init(&c0.full, 1);
     fence_mbar_init();
     c0.progress = 0;
@@ -534,13 +536,14 @@ zvc_status split_occupancy(uint32_t k, uint32_t cap, uint32_t wpc, int* occ) {
 }
 
 // With short chunks (a mean of at most 1/6 of the largest, or chunks of at most 1024
-// elements) in a launch of two waves or more, the chunks per CTA (1, 2 or 4; one walker
-// warp walks them all, one lane each) that keep the most chunks in flight per SM, preferring more per CTA on a tie: the
-// kernel is then bound by the instructions it issues, and a shared walker warp issues a
-// quarter of them per chunk. Otherwise one chunk per CTA: a CTA frees its shared memory
-// only when its slowest chunk is done. Then widens *cap to the largest buffer that keeps
-// the CTAs per SM the launch needs: as many as fit, or fewer when fewer hold every chunk in
-// as many waves. A larger buffer stages fewer chunks in pieces.
+// elements) in a launch of two waves or more, picks the chunks per CTA (1, 2 or 4; one
+// walker warp walks them all, one lane each) that keep the most chunks in flight per SM,
+// preferring more per CTA on a tie: the kernel is then bound by the instructions it
+// issues, and a shared walker warp issues a quarter of them per chunk. Otherwise one
+// chunk per CTA: a CTA frees its shared memory only when its slowest chunk is done. Then
+// widens *cap to the largest buffer that keeps the CTAs per SM the launch needs: as many
+// as fit, or fewer when fewer hold every chunk in as many waves. A larger buffer stages
+// fewer chunks in pieces.
 template <int MAXT, bool SMALL>
 zvc_status plan_split(const DeviceLimits& d, uint64_t chunks, uint64_t mean, uint32_t wpc,
                       uint32_t full_cap, uint32_t* cap, uint32_t* chunks_per_cta) {
@@ -566,8 +569,10 @@ zvc_status plan_split(const DeviceLimits& d, uint64_t chunks, uint64_t mean, uin
   const uint64_t ctas = ceil_div_u64(chunks, k);
   const uint64_t waves = ceil_div_u64(ctas, (uint64_t)occ * d.sms);
   const uint64_t need = ceil_div_u64(ctas, waves * d.sms);  // CTAs per SM, at most occ
-  const uint64_t per_cta = min((uint64_t)d.smem_per_sm / need, (uint64_t)d.smem_per_cta_max + d.reserved_per_cta);
-  const uint64_t fixed = (uint64_t)d.reserved_per_cta + 4ull * k * (kCtlWords + round_up_u64(2ull * wpc, 4));
+  const uint64_t per_cta =
+      min((uint64_t)d.smem_per_sm / need, (uint64_t)d.smem_per_cta_max + d.reserved_per_cta);
+  const uint64_t fixed =
+      (uint64_t)d.reserved_per_cta + 4ull * k * (kCtlWords + round_up_u64(2ull * wpc, 4));
   if (per_cta <= fixed + 16ull * k) return ZVC_OK;
   uint64_t c = ((per_cta - fixed) / (4ull * k)) & ~3ull;
   c = c < full_cap ? c : (uint64_t)full_cap;
@@ -613,8 +618,8 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
       decompress_kernel<MAXT, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)min(most, (uint64_t)d.smem_per_cta_max));
   if (e != cudaSuccess) return cuda_failure(e);
-  e = cudaFuncSetAttribute(decompress_kernel<MAXT, SMALL>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           100);
+  e = cudaFuncSetAttribute(decompress_kernel<MAXT, SMALL>,
+                           cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return cuda_failure(e);
   args.cap_words = full_cap;
   if (chunks > 0) {
@@ -628,7 +633,8 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
         min((uint64_t)full_cap, in_bytes > fixed ? (in_bytes - fixed) / 4 / chunks : 0);
     const uint64_t want = round_up_u64(mean * kCapSlackNum / kCapSlackDen + kCapExtraWords, 4);
     args.cap_words = (uint32_t)min((uint64_t)full_cap, max((uint64_t)kCapMinWords, want));
-    st = plan_split<MAXT, SMALL>(d, chunks, mean, wpc, full_cap, &args.cap_words, &args.chunks_per_cta);
+    st = plan_split<MAXT, SMALL>(d, chunks, mean, wpc, full_cap, &args.cap_words,
+                                 &args.chunks_per_cta);
     if (st != ZVC_OK) return st;
   }
   args.meta_offset_words = args.cap_words;
@@ -647,7 +653,8 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
 template <int MAXT>
 zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, uint32_t T,
                     bool batched, uint32_t C, uint8_t* ws, cudaStream_t stream) {
-  if (C <= kSmallChunkElems) return launch_k<MAXT, true>(in, in_bytes, ts, T, batched, C, ws, stream);
+  if (C <= kSmallChunkElems)
+    return launch_k<MAXT, true>(in, in_bytes, ts, T, batched, C, ws, stream);
   return launch_k<MAXT, false>(in, in_bytes, ts, T, batched, C, ws, stream);
 }
 
