@@ -18,7 +18,8 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libzvc_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 SOURCES = ["zvc_compress.cu", "zvc_decompress.cu", "zvc_api.cu", "zvc_static.cu", "zvc_rle.cu"]
-HEADERS = [os.path.join(CSRC, "zvc_internal.cuh"), os.path.join(INCLUDE, "zvc.h")]
+HEADERS = [os.path.join(CSRC, "zvc_internal.cuh"), os.path.join(CSRC, "zvc_plan.h"),
+           os.path.join(INCLUDE, "zvc.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--cudart", "shared",
          f"-I{INCLUDE}"]

@@ -26,6 +26,7 @@
 #include <atomic>
 
 #include "zvc_internal.cuh"
+#include "zvc_plan.h"
 
 namespace zvc {
 namespace {
@@ -41,7 +42,7 @@ struct DecompressCtl {
   uint32_t expanded;  // the windows before it are read out of the buffer (scatterer -> walker)
   uint32_t pad[2];
 };
-constexpr uint32_t kCtlWords = 8;  // sizeof(DecompressCtl) / 4: the buffer stays 16-byte aligned
+constexpr uint32_t kCtlWords = plan::kSlotCtlWords;  // sizeof(DecompressCtl) / 4: 16-byte aligned
 static_assert(sizeof(DecompressCtl) == 4 * kCtlWords, "control words");
 constexpr uint32_t kPublishEvery = 16;  // the scatterer expands 16 windows at a time
 constexpr uint32_t kPollSleepNs = 32;   // the scatterer's sleep between polls of the table
@@ -436,14 +437,8 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
 }
 
 // Every chunk gets a scatterer warp of its own and a lane of the CTA's walker warp; the
-// host picks the chunks per CTA. A chunk's buffer: 5/4 of the mean chunk + 64 words, at
-// least 1024 words (a piece then holds at least 31 windows), at most the largest chunk.
-constexpr uint64_t kCapSlackNum = 5, kCapSlackDen = 4, kCapExtraWords = 64;
-constexpr uint32_t kCapMinWords = 1024;
-constexpr uint32_t kSplitMaxChunksPerCta = 4;  // chunks one walker warp walks at once
-constexpr uint64_t kMultiMeanDiv = 6;          // several chunks per CTA: mean <= largest / 6,
-constexpr uint32_t kMultiAnyWords = 1060;      // or chunks of at most 1024 elements
-constexpr uint32_t kMaxThreads = 32 * (1 + kSplitMaxChunksPerCta);
+// host picks the chunks per CTA and the chunk buffer's size (zvc_plan.h).
+constexpr uint32_t kMaxThreads = 32 * (1 + plan::kMaxChunksPerCta);
 // Chunks of at most 1024 elements are bound by the chunks in flight per SM, which registers
 // limit: their kernel is built for 10 CTAs of kMaxThreads per SM (32 registers; measured
 // 8% faster there, and 7-22% slower for 4096-element chunks).
@@ -486,17 +481,8 @@ __global__ void __launch_bounds__(kMaxThreads, SMALL ? kSmallMinCtas : 0)
   }
 }
 
-// Shared memory of a chunk whose buffer holds cap words.
-inline uint64_t split_smem_bytes(uint32_t cap, uint32_t wpc) {
-  return 4ull * round_up_u64(kCtlWords + (uint64_t)cap + 2ull * wpc, 4);
-}
-
-struct DeviceLimits {
-  int sms, smem_per_sm, reserved_per_cta, smem_per_cta_max;
-};
-
 // The device's SM count and shared memory, read once per device.
-zvc_status device_limits(DeviceLimits* d) {
+zvc_status device_limits(plan::Limits* d) {
   constexpr int kMaxDevices = 64;
   static std::atomic<int> sms_of[kMaxDevices], smem_of[kMaxDevices], reserved_of[kMaxDevices],
       cta_max_of[kMaxDevices];
@@ -525,64 +511,6 @@ zvc_status device_limits(DeviceLimits* d) {
   return ZVC_OK;
 }
 
-// CTAs of k chunks with buffers of cap words that fit on one SM.
-template <int MAXT, bool SMALL>
-zvc_status split_occupancy(uint32_t k, uint32_t cap, uint32_t wpc, int* occ) {
-  *occ = 0;
-  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      occ, decompress_kernel<MAXT, SMALL>, (int)(32 * (1 + k)),
-      (size_t)(k * split_smem_bytes(cap, wpc)));
-  return e == cudaSuccess ? ZVC_OK : cuda_failure(e);
-}
-
-// With short chunks (a mean of at most 1/6 of the largest, or chunks of at most 1024
-// elements) in a launch of two waves or more, picks the chunks per CTA (1, 2 or 4; one
-// walker warp walks them all, one lane each) that keep the most chunks in flight per SM,
-// preferring more per CTA on a tie: the kernel is then bound by the instructions it
-// issues, and a shared walker warp issues a quarter of them per chunk. Otherwise one
-// chunk per CTA: a CTA frees its shared memory only when its slowest chunk is done. Then
-// widens *cap to the largest buffer that keeps the CTAs per SM the launch needs: as many
-// as fit, or fewer when fewer hold every chunk in as many waves. A larger buffer stages
-// fewer chunks in pieces.
-template <int MAXT, bool SMALL>
-zvc_status plan_split(const DeviceLimits& d, uint64_t chunks, uint64_t mean, uint32_t wpc,
-                      uint32_t full_cap, uint32_t* cap, uint32_t* chunks_per_cta) {
-  zvc_status st;
-  uint32_t k = 1;
-  int occ = 0;
-  if ((st = split_occupancy<MAXT, SMALL>(1, *cap, wpc, &occ)) != ZVC_OK) return st;
-  const bool short_chunks = mean * kMultiMeanDiv <= full_cap || full_cap <= kMultiAnyWords;
-  const bool waves2 = occ > 0 && chunks >= 2ull * (uint64_t)occ * d.sms;
-  uint64_t best = (uint64_t)occ;
-  for (uint32_t kk = 2; short_chunks && waves2 && kk <= kSplitMaxChunksPerCta; kk *= 2) {
-    if (kk * split_smem_bytes(*cap, wpc) > (uint64_t)d.smem_per_cta_max) break;
-    int o = 0;
-    if ((st = split_occupancy<MAXT, SMALL>(kk, *cap, wpc, &o)) != ZVC_OK) return st;
-    if ((uint64_t)o * kk >= best && o > 0) {
-      best = (uint64_t)o * kk;
-      k = kk;
-      occ = o;
-    }
-  }
-  *chunks_per_cta = k;
-  if (occ <= 0 || d.sms <= 0 || *cap >= full_cap) return ZVC_OK;
-  const uint64_t ctas = ceil_div_u64(chunks, k);
-  const uint64_t waves = ceil_div_u64(ctas, (uint64_t)occ * d.sms);
-  const uint64_t need = ceil_div_u64(ctas, waves * d.sms);  // CTAs per SM, at most occ
-  const uint64_t per_cta =
-      min((uint64_t)d.smem_per_sm / need, (uint64_t)d.smem_per_cta_max + d.reserved_per_cta);
-  const uint64_t fixed =
-      (uint64_t)d.reserved_per_cta + 4ull * k * (kCtlWords + round_up_u64(2ull * wpc, 4));
-  if (per_cta <= fixed + 16ull * k) return ZVC_OK;
-  uint64_t c = ((per_cta - fixed) / (4ull * k)) & ~3ull;
-  c = c < full_cap ? c : (uint64_t)full_cap;
-  if (c <= *cap) return ZVC_OK;
-  int o2 = 0;
-  if ((st = split_occupancy<MAXT, SMALL>(k, (uint32_t)c, wpc, &o2)) != ZVC_OK) return st;
-  if ((uint64_t)o2 >= need) *cap = (uint32_t)c;
-  return ZVC_OK;
-}
-
 template <int MAXT, bool SMALL>
 zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, uint32_t T,
                     bool batched, uint32_t C, uint8_t* ws, cudaStream_t stream) {
@@ -605,15 +533,13 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   args.total_chunks = chunks;
   args.total_items = chunks + (batched && T == 0 ? 1 : T);
   const uint32_t wpc = C / kWindow;
-  // the largest valid chunk (C/32 masks + C words) at any 16-byte phase
-  const uint32_t full_cap = (uint32_t)round_up_u64(wpc + C + 3ull, 4);
-  args.chunks_per_cta = 1u;
-  DeviceLimits d;
+  const uint32_t full_cap = plan::full_cap_words(C);
+  plan::Limits d;
   zvc_status st = device_limits(&d);
   if (st != ZVC_OK) return st;
   // the most shared memory a CTA of this chunk size can ask for (within the device's
   // limit), and all of the SM's unified memory as shared memory
-  const uint64_t most = split_smem_bytes(full_cap, wpc) * kSplitMaxChunksPerCta;
+  const uint64_t most = plan::slot_bytes(full_cap, C) * plan::kMaxChunksPerCta;
   cudaError_t e = cudaFuncSetAttribute(
       decompress_kernel<MAXT, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)min(most, (uint64_t)d.smem_per_cta_max));
@@ -621,22 +547,24 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   e = cudaFuncSetAttribute(decompress_kernel<MAXT, SMALL>,
                            cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return cuda_failure(e);
-  args.cap_words = full_cap;
-  if (chunks > 0) {
-    // A CTA's shared memory is fixed at launch and sets how many chunks are in flight per
-    // SM, so the buffer is sized from the mean chunk length (the stream's size less its
-    // headers and tables): chunks up to 5/4 of the mean (+64 words) go in one piece. Then
-    // it is widened as far as the CTAs per SM the launch needs allow.
-    const uint64_t fixed = (batched ? 16ull + 8ull * ((uint64_t)T + 1) : 0ull) + 32ull * T +
-                           8ull * chunks;
-    const uint64_t mean =
-        min((uint64_t)full_cap, in_bytes > fixed ? (in_bytes - fixed) / 4 / chunks : 0);
-    const uint64_t want = round_up_u64(mean * kCapSlackNum / kCapSlackDen + kCapExtraWords, 4);
-    args.cap_words = (uint32_t)min((uint64_t)full_cap, max((uint64_t)kCapMinWords, want));
-    st = plan_split<MAXT, SMALL>(d, chunks, mean, wpc, full_cap, &args.cap_words,
-                                 &args.chunks_per_cta);
-    if (st != ZVC_OK) return st;
-  }
+  // the buffer's size and the chunks per CTA, with the occupancy the runtime reports
+  cudaError_t occ_err = cudaSuccess;
+  auto occ = [&](uint32_t k, uint32_t cap) -> int {
+    int n = 0;
+    const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, decompress_kernel<MAXT, SMALL>, (int)(32 * (1 + k)),
+        (size_t)(k * plan::slot_bytes(cap, C)));
+    if (r != cudaSuccess) {
+      occ_err = r;
+      return -1;
+    }
+    return n;
+  };
+  plan::Plan pl;
+  if (!plan::decompress_plan(chunks, in_bytes, T, batched, C, d, occ, &pl))
+    return cuda_failure(occ_err);
+  args.cap_words = pl.cap_words;
+  args.chunks_per_cta = pl.chunks_per_cta;
   args.meta_offset_words = args.cap_words;
   args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.cap_words + 2ull * wpc, 4);
   const uint64_t smem = 4ull * args.slot_words * args.chunks_per_cta;

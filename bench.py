@@ -86,7 +86,7 @@ def parse_args(argv=None):
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_traffic.json")
 KERNEL_SOURCES = {
     "compress_kernel": ["zvc_compress.cu", "zvc_internal.cuh"],
-    "decompress_kernel": ["zvc_decompress.cu", "zvc_internal.cuh"],
+    "decompress_kernel": ["zvc_decompress.cu", "zvc_plan.h", "zvc_internal.cuh"],
 }
 
 
