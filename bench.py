@@ -52,6 +52,9 @@ def parse_args(argv=None):
     p.add_argument("--profile", choices=["compress", "decompress"],
                    help="run a few launches of one kernel on AlexNet layer 0 (149 MB) and "
                         "exit: the small case for ncu captures")
+    p.add_argument("--profile-density", type=float, default=None, metavar="D",
+                   help="with --profile: a flat map of the same size with a fraction D of "
+                        "i.i.d. non-zero words, instead of AlexNet layer 0")
     p.add_argument("--train", action="store_true",
                    help="training step of a VGG-style CNN with its saved activations kept, "
                         "offloaded compressed to host memory, or kept compressed in HBM; "
@@ -627,8 +630,9 @@ def measure_e2e(args, zvc, torch, xs, ns, C, dev, stream, step, hsize):
 
 def run_profile_case(args):
     """Warm-up launches, then three timed groups of ten back-to-back launches of one kernel
-    on AlexNet layer 0 (batch 128 x 96 x 55 x 55 fp32, 60% non-zero); prints the mean
-    CUDA-event time per launch of each group."""
+    on AlexNet layer 0 (batch 128 x 96 x 55 x 55 fp32, 60% non-zero), or with
+    --profile-density D on a flat map of as many words with a fraction D non-zero; prints
+    the mean CUDA-event time per launch of each group."""
     import torch
 
     from activation_sparsity_compression_gb300 import build as zbuild
@@ -639,8 +643,12 @@ def run_profile_case(args):
     C = args.chunk_elems
     g = torch.Generator(device="cuda").manual_seed(1)
     c, h, w, d = workloads.ALEXNET_LAYERS[0]
-    b = torch.tensor(workloads.alexnet_biases(c, d, 1), device="cuda").view(1, c, 1, 1)
-    x = torch.relu_(torch.randn((128, c, h, w), generator=g, device="cuda").add_(b))
+    if args.profile_density is None:
+        b = torch.tensor(workloads.alexnet_biases(c, d, 1), device="cuda").view(1, c, 1, 1)
+        x = torch.relu_(torch.randn((128, c, h, w), generator=g, device="cuda").add_(b))
+    else:
+        x = workloads.density_sweep(args.profile_density, "iid", device="cuda",
+                                    n=128 * c * h * w)[0]
     n = x.numel()
     out = torch.empty(zvc.zvc_size_bound(n, C), dtype=torch.uint8, device="cuda")
     size = torch.zeros(1, dtype=torch.int64, device="cuda")
@@ -674,7 +682,8 @@ def run_profile_case(args):
     if args.profile == "decompress":
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
     moved = 4 * n + S
-    print(json.dumps({"profile": args.profile, "n": n, "stream_bytes": S,
+    print(json.dumps({"profile": args.profile, "density": args.profile_density, "n": n,
+                      "stream_bytes": S,
                       "ms": times[1:], "hbm_gbs": [moved / (t / 1e3) / 1e9 for t in times[1:]]}))
     return 0
 
