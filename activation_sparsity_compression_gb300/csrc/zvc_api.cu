@@ -4,6 +4,7 @@
 // pointers, sizes and copies.
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -103,16 +104,27 @@ bool layout_fits(const WsLayout& l, const SegPlan& p) {
 
 // Side stream (the copy stream) for the pipeline, one per device, created on first use,
 // and per workspace the events of its staging buffers: the kernel and the copy that last
-// used buffer b.
+// used buffer b. A call holds the per-device mutex only to look its workspace's events up
+// and to enqueue a group of copy-stream operations (wait, copy, record) in one piece; it
+// never holds it while it blocks, so a zvc_prefetch from one thread is not queued behind
+// a zvc_offload that waits for a kernel on another.
 struct Slots {
-  cudaEvent_t kernel_done[kPipeDepth];
-  cudaEvent_t copy_done[kPipeDepth];
+  cudaEvent_t kernel_done[kPipeDepth] = {};
+  cudaEvent_t copy_done[kPipeDepth] = {};
+  // Destroying an event whose work is still pending is allowed: CUDA releases it once
+  // the work completes.
+  ~Slots() {
+    for (int b = 0; b < kPipeDepth; ++b) {
+      if (kernel_done[b]) cudaEventDestroy(kernel_done[b]);
+      if (copy_done[b]) cudaEventDestroy(copy_done[b]);
+    }
+  }
 };
 
 struct Pipe {
   cudaStream_t side = nullptr;
   cudaEvent_t joined = nullptr;
-  std::map<uintptr_t, Slots> slots;  // by workspace address
+  std::map<uintptr_t, std::shared_ptr<Slots>> slots;  // by workspace address
   std::mutex mu;
 };
 
@@ -138,31 +150,36 @@ zvc_status get_pipe(Pipe** out) {
   return ZVC_OK;
 }
 
-// The staging-buffer events of workspace ws (created on first use). Called with pipe->mu
-// held. A process that cycles through very many workspaces drops the whole table once it
-// holds 4096 of them, after waiting for every event in it.
-zvc_status slots_for(Pipe* pipe, const void* ws, Slots** out) {
+// The staging-buffer events of workspace ws (created on first use). Takes pipe->mu. A
+// process that cycles through very many workspaces drops, once the table holds 4096 of
+// them, every entry no call is using, after waiting for its events: a later call through
+// such a workspace starts from fresh events, with the earlier work already done.
+zvc_status slots_for(Pipe* pipe, const void* ws, std::shared_ptr<Slots>* out) {
+  std::lock_guard<std::mutex> lk(pipe->mu);
   const uintptr_t key = reinterpret_cast<uintptr_t>(ws);
   auto it = pipe->slots.find(key);
   if (it == pipe->slots.end()) {
     if (pipe->slots.size() >= 4096) {
-      for (auto& kv : pipe->slots)
-        for (int b = 0; b < kPipeDepth; ++b) {
-          ZVC_CUDA_TRY(cudaEventSynchronize(kv.second.kernel_done[b]));
-          ZVC_CUDA_TRY(cudaEventSynchronize(kv.second.copy_done[b]));
-          cudaEventDestroy(kv.second.kernel_done[b]);
-          cudaEventDestroy(kv.second.copy_done[b]);
+      for (auto j = pipe->slots.begin(); j != pipe->slots.end();) {
+        if (j->second.use_count() != 1) {
+          ++j;
+          continue;
         }
-      pipe->slots.clear();
+        for (int b = 0; b < kPipeDepth; ++b) {
+          ZVC_CUDA_TRY(cudaEventSynchronize(j->second->kernel_done[b]));
+          ZVC_CUDA_TRY(cudaEventSynchronize(j->second->copy_done[b]));
+        }
+        j = pipe->slots.erase(j);
+      }
     }
-    Slots sl;
+    auto sl = std::make_shared<Slots>();
     for (int b = 0; b < kPipeDepth; ++b) {
-      ZVC_CUDA_TRY(cudaEventCreateWithFlags(&sl.kernel_done[b], cudaEventDisableTiming));
-      ZVC_CUDA_TRY(cudaEventCreateWithFlags(&sl.copy_done[b], cudaEventDisableTiming));
+      ZVC_CUDA_TRY(cudaEventCreateWithFlags(&sl->kernel_done[b], cudaEventDisableTiming));
+      ZVC_CUDA_TRY(cudaEventCreateWithFlags(&sl->copy_done[b], cudaEventDisableTiming));
     }
-    it = pipe->slots.emplace(key, sl).first;
+    it = pipe->slots.emplace(key, std::move(sl)).first;
   }
-  *out = &it->second;
+  *out = it->second;
   return ZVC_OK;
 }
 
@@ -384,8 +401,7 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
   Pipe* pipe = nullptr;
   zvc_status st = get_pipe(&pipe);
   if (st != ZVC_OK) return st;
-  std::lock_guard<std::mutex> lk(pipe->mu);
-  Slots* sl = nullptr;
+  std::shared_ptr<Slots> sl;
   if ((st = slots_for(pipe, d_ws, &sl)) != ZVC_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -407,10 +423,13 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
     const uint64_t sz = *reinterpret_cast<volatile uint64_t*>(H + 16 + 8 * k);
     if (sz == 0 || sz > L.stage || pos + sz > h_cap) return read_latched(d_ws);
     offs[k] = pos;
-    ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, sl->kernel_done[b], 0));
-    ZVC_CUDA_TRY(cudaMemcpyAsync(H + pos, ws + L.kernel_ws + b * L.stage, sz,
-                                 cudaMemcpyDeviceToHost, pipe->side));
-    ZVC_CUDA_TRY(cudaEventRecord(sl->copy_done[b], pipe->side));
+    {
+      std::lock_guard<std::mutex> lk(pipe->mu);  // the three copy-stream steps in one piece
+      ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, sl->kernel_done[b], 0));
+      ZVC_CUDA_TRY(cudaMemcpyAsync(H + pos, ws + L.kernel_ws + b * L.stage, sz,
+                                   cudaMemcpyDeviceToHost, pipe->side));
+      ZVC_CUDA_TRY(cudaEventRecord(sl->copy_done[b], pipe->side));
+    }
     pos += sz;
     return ZVC_OK;
   };
@@ -477,8 +496,7 @@ zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint
   Pipe* pipe = nullptr;
   zvc_status st = get_pipe(&pipe);
   if (st != ZVC_OK) return st;
-  std::lock_guard<std::mutex> lk(pipe->mu);
-  Slots* sl = nullptr;
+  std::shared_ptr<Slots> sl;
   if ((st = slots_for(pipe, d_ws, &sl)) != ZVC_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -491,9 +509,12 @@ zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint
     const int b = (int)(k % kPipeDepth);
     const uint64_t a = get_u64(H + 16 + 8 * k), sz = get_u64(H + 24 + 8 * k) - a;
     uint8_t* stage = ws + L.kernel_ws + b * L.stage;
-    ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, sl->kernel_done[b], 0));
-    ZVC_CUDA_TRY(cudaMemcpyAsync(stage, H + a, sz, cudaMemcpyHostToDevice, pipe->side));
-    ZVC_CUDA_TRY(cudaEventRecord(sl->copy_done[b], pipe->side));
+    {
+      std::lock_guard<std::mutex> lk(pipe->mu);  // the three copy-stream steps in one piece
+      ZVC_CUDA_TRY(cudaStreamWaitEvent(pipe->side, sl->kernel_done[b], 0));
+      ZVC_CUDA_TRY(cudaMemcpyAsync(stage, H + a, sz, cudaMemcpyHostToDevice, pipe->side));
+      ZVC_CUDA_TRY(cudaEventRecord(sl->copy_done[b], pipe->side));
+    }
     ZVC_CUDA_TRY(cudaStreamWaitEvent(s, sl->copy_done[b], 0));
     const uint64_t nk = (k + 1 < S) ? p.seg : n - k * p.seg;
     const TensorOut t{out + k * p.seg, nk};

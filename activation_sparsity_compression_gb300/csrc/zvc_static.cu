@@ -9,13 +9,13 @@
 // that is part of the library image: every GPU that loads the library holds
 // kStaticScratchBytes of it until the process exits.
 //
-// The array is shared by every call on a device and keeps the previous call's contents;
-// each call clears the parts that must start at zero before its kernel runs, except the
-// error latch, which keeps a failure until zvc_compress_static_get_error reads it. Two
-// calls whose work overlaps on the GPU (different streams, no ordering between them) use
-// the same scratch and race: order them on one stream or synchronise between them.
-#include <mutex>
-
+// The array is shared by every call on a device and keeps the previous call's contents.
+// Nothing in it is cleared between calls: every compress launch tags the status words it
+// writes with a number drawn anew for that launch, so entries left by earlier calls never
+// match the new call's. Only the error latch carries over from one call to the next: it
+// keeps a failure until zvc_compress_static_get_error reads and clears it. Two calls whose
+// work overlaps on the GPU (different streams, no ordering between them) use the same
+// scratch and race: order them on one stream or synchronise between them.
 #include "zvc_internal.cuh"
 
 namespace {
@@ -30,26 +30,16 @@ static_assert(zvc::kStatusOffset + 8 * (ZVC_STATIC_MAX_ELEMS / zvc::kTileElems) 
 
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
 // The device address of g_static_scratch on the current device. In host code the name
 // g_static_scratch is only a host-side stand-in for the symbol, so the address is looked
-// up once per device, with that device current, and cached.
+// up with the device current, on every call: a cached address would dangle once the
+// device's context is torn down (cudaDeviceReset) and the module loaded again. The first
+// lookup on a device also loads the library's device code there.
 zvc_status scratch_for_current_device(uint8_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
   if (e != cudaSuccess) return zvc::cuda_failure(e);
-  if (dev < 0 || dev >= kMaxDevices) return ZVC_ERR_INVALID_ARG;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return zvc::cuda_failure(e);
-    g_scratch_ptr[dev] = p;
-  }
-  *out = static_cast<uint8_t*>(g_scratch_ptr[dev]);
+  *out = static_cast<uint8_t*>(p);
   return ZVC_OK;
 }
 

@@ -69,20 +69,30 @@ typedef int zvc_status;
 #define ZVC_WORKSPACE_ALIGN 256u
 
 /* Worst-case (all words non-zero) size in bytes of one stream of n words:
- * 32 + 8*ceil(n/C) + 4*ceil(n/32) + 4*n. Returns 0 if chunk_elems is invalid. */
+ * 32 + 8*ceil(n/C) + 4*ceil(n/32) + 4*n. Cites section V.A "Compression Algorithm": a
+ * window costs its 4-byte mask plus 4 bytes per non-zero word, so a dense window grows
+ * by one word. Returns 0 if chunk_elems is invalid. */
 uint64_t zvc_size_bound(uint64_t n, uint32_t chunk_elems);
 
 /* Worst-case size of a batch of T streams: 16 + 8*(T+1) + sum of zvc_size_bound.
- * ns is a host array of T word counts. Returns 0 on invalid arguments. */
+ * Cites section V.A "Compression Algorithm" per stream; the batch framing (one stream
+ * per tensor behind a table of stream offsets) is this library's reading, the paper has
+ * no counterpart for it. ns is a host array of T word counts. Returns 0 on invalid
+ * arguments. */
 uint64_t zvc_batch_size_bound(const uint64_t* ns, uint32_t T, uint32_t chunk_elems);
 
 /* Workspace bytes for zvc_compress / zvc_decompress of n words: the latched error word,
- * then one look-back status word per 4096-word tile. Each compress launch tags the status
- * words it writes with a number of its own, so a workspace needs no clearing between
- * calls; only its error word must start at zero (see the conventions above). */
+ * then one look-back status word per 4096-word tile. Cites section V.B "Compressing DMA
+ * Engine Architecture": the compressed offsets are prefix sums of the masks' population
+ * counts; across tiles that prefix sum is carried by these status words. Each compress
+ * launch tags the status words it writes with a number of its own, so a workspace needs
+ * no clearing between calls; only its error word must start at zero (see the conventions
+ * above). */
 uint64_t zvc_workspace_size(uint64_t n, uint32_t chunk_elems);
 
-/* Workspace bytes for the batched calls over the T tensors in ns (host array). */
+/* Workspace bytes for the batched calls over the T tensors in ns (host array): as
+ * zvc_workspace_size (section V.B, prefix sums across tiles) for every tile of every
+ * tensor, plus one start word per tensor for the batch framing. */
 uint64_t zvc_batch_workspace_size(const uint64_t* ns, uint32_t T, uint32_t chunk_elems);
 
 /* Compress n words at d_in into one stream at d_out (section V.A; the size report of the
@@ -99,9 +109,12 @@ zvc_status zvc_compress(const void* d_in, uint64_t n, uint32_t chunk_elems, void
  * fails once memory is fully reserved. The paper has no counterpart; this is a library
  * convenience. Same inputs, output and stream as zvc_compress, minus d_ws/ws_bytes: the
  * scratch is one static device array of about 1 MiB that every GPU loading the library
- * keeps until exit. Limits: n <= ZVC_STATIC_MAX_ELEMS, else ZVC_ERR_INVALID_ARG. The
- * first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * and caches it. The call allocates nothing. All calls on a device share the array, so
+ * keeps until exit. Limits: n <= ZVC_STATIC_MAX_ELEMS, else ZVC_ERR_INVALID_ARG. Every
+ * call looks up the array's device address on the current device (cudaGetSymbolAddress);
+ * the first call on a device also loads the library's device code there, so make it
+ * before any stream capture. The call allocates nothing. All calls on a device share the
+ * array, and nothing in it is cleared between calls (each launch tags its entries with a
+ * number of its own; only the error latch below carries over), so
  * calls whose GPU work overlaps (unordered streams) race and must be ordered by the
  * caller. A failure on the device (a wait that gave up) is latched in the array, where
  * it stays until zvc_compress_static_get_error() reads it; the stream's bytes and
@@ -111,7 +124,8 @@ zvc_status zvc_compress_static(const void* d_in, uint64_t n, uint32_t chunk_elem
                                uint64_t out_cap, uint64_t* d_out_size, void* stream);
 
 /* The status latched by zvc_compress_static calls on the current device since the last
- * read (ZVC_OK if none): synchronises `stream`, reads the latch and clears it. */
+ * read (ZVC_OK if none): synchronises `stream`, reads the latch and clears it. The paper
+ * has no counterpart, as for zvc_compress_static. */
 zvc_status zvc_compress_static_get_error(void* stream);
 
 /* Decompress the stream of in_bytes bytes at d_in into n words at d_out (inverse of
@@ -122,29 +136,40 @@ zvc_status zvc_compress_static_get_error(void* stream);
 zvc_status zvc_decompress(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,
                           uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream);
 
-/* Compress T tensors in one launch into one batch at d_out. d_ins (device pointers) and
- * ns are HOST arrays of T entries; T <= ZVC_MAX_BATCH. out_cap >= zvc_batch_size_bound.
- * The batch's total byte count goes to *d_out_size (device, may be NULL). */
+/* Compress T tensors in one launch into one batch at d_out: section V.A "Compression
+ * Algorithm" applied to every tensor, with one prefix sum (section V.B) over the tiles of
+ * all of them; section V.D "Software Interface" offloads every layer's activation maps,
+ * and this call serves many small maps with one launch. The per-tensor offset table is
+ * this library's framing. d_ins (device pointers) and ns are HOST arrays of T entries;
+ * T <= ZVC_MAX_BATCH. out_cap >= zvc_batch_size_bound. The batch's total byte count goes
+ * to *d_out_size (device, may be NULL). */
 zvc_status zvc_compress_batched(const void* const* d_ins, const uint64_t* ns, uint32_t T,
                                 uint32_t chunk_elems, void* d_out, uint64_t out_cap,
                                 uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
                                 void* stream);
 
-/* Decompress a batch of in_bytes bytes into T tensors. d_outs (device pointers) and ns are
- * HOST arrays of T entries. Corruption is latched as for zvc_decompress. */
+/* Decompress a batch of in_bytes bytes into T tensors (the inverse of section V.A for
+ * every stream of the batch, found through its per-tensor offset table). d_outs (device
+ * pointers) and ns are HOST arrays of T entries. Corruption is latched as for
+ * zvc_decompress. */
 zvc_status zvc_decompress_batched(const void* d_in, uint64_t in_bytes, void* const* d_outs,
                                   const uint64_t* ns, uint32_t T, uint32_t chunk_elems,
                                   void* d_ws, uint64_t ws_bytes, void* stream);
 
 /* Segment length (words) that zvc_offload uses for a tensor of n words: n cut into
  * ceil(n / 2^25) equal parts, rounded up to whole chunks (at most about 32 Mi words,
- * 128 MiB of fp32). */
+ * 128 MiB of fp32). Cites section V.D "Software Interface": compression throughput must
+ * match the transfer path, so the copy of one segment overlaps the compression of the
+ * next; the segment length itself is this library's choice. */
 uint64_t zvc_offload_segment_elems(uint64_t n, uint32_t chunk_elems);
 
-/* Host bytes zvc_offload may need: the batch bound over its segments. */
+/* Host bytes zvc_offload may need: the batch bound over its segments. Cites section V.D
+ * "Software Interface": vDNN sizes its host allocations from the compressed size; this is
+ * the worst case, before the size is known. */
 uint64_t zvc_offload_host_bound(uint64_t n, uint32_t chunk_elems);
 
-/* Workspace bytes for zvc_offload / zvc_prefetch: device staging for the pipelined
+/* Workspace bytes for zvc_offload / zvc_prefetch (section V.D "Software Interface":
+ * offload and prefetch with cudaMemcpyAsync): device staging for the pipelined
  * segments plus the per-segment kernel workspace. Where these sit inside a workspace
  * depends on its size alone, so one workspace of W bytes serves, in any order and on any
  * stream, every tensor whose zvc_offload_workspace_size is at most W; a smaller W returns
@@ -177,7 +202,9 @@ zvc_status zvc_offload(const void* d_in, uint64_t n, uint32_t chunk_elems, void*
                        void* stream);
 
 /* Offload join: work enqueued on `stream` after this call waits for every copy that
- * zvc_offload has enqueued on this device so far. */
+ * zvc_offload has enqueued on this device so far. Cites section V.D "Software Interface":
+ * the copies are asynchronous (cudaMemcpyAsync), so a caller that reads the host copy
+ * orders itself after them through this call. */
 zvc_status zvc_offload_join(void* stream);
 
 /* Prefetch (section V.D: vDNN prefetches offloaded activations before backward
@@ -194,14 +221,17 @@ zvc_status zvc_offload_join(void* stream);
 zvc_status zvc_prefetch(const void* h_pinned, uint64_t h_size, void* d_out, uint64_t n,
                         uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream);
 
-/* Self-test of the device-side wait limit: launches the decoupled look-back of a tile
- * whose predecessor never publishes, with a wait limit of limit_ns (0 < limit_ns <= 1 s).
+/* Self-test of the device-side wait limit; the paper has no counterpart (its engine is
+ * hardware): launches the decoupled look-back of a tile whose predecessor never
+ * publishes, with a wait limit of limit_ns (0 < limit_ns <= 1 s).
  * The wait gives up and latches ZVC_ERR_TIMEOUT in d_ws (read it with zvc_get_error);
  * the context stays usable. d_ws needs at least 1024 bytes. */
 zvc_status zvc_selftest_wait_timeout(void* d_ws, uint64_t ws_bytes, uint64_t limit_ns,
                                      void* stream);
 
-/* Kernel tracing. zvc_trace_start() makes every following kernel launch of this library
+/* Kernel tracing; the paper has no counterpart (section V.D notes that its own evaluation
+ * measured copy latencies on the host). zvc_trace_start() makes every following kernel
+ * launch of this library
  * (on any stream, from any call, including the launches inside zvc_offload/zvc_prefetch)
  * record a CUDA event pair on its own stream. zvc_trace_stop() waits for those events,
  * stops tracing and writes, per kernel kind (index 0 = compress, 1 = decompress), the
@@ -211,7 +241,9 @@ zvc_status zvc_trace_start(void);
 zvc_status zvc_trace_stop(uint64_t* launches, double* device_ms);
 
 /* Synchronises `stream`, returns the first device-side error latched in d_ws since the
- * last call (ZVC_OK if none) and clears it. */
+ * last call (ZVC_OK if none) and clears it. Cites section V.D "Software Interface": the
+ * proposed compressed copy call returns a result to its caller; errors that only the
+ * device can see (a corrupt stream, a wait that gave up) reach the caller through here. */
 zvc_status zvc_get_error(void* d_ws, void* stream);
 
 /* ---------------------------------------------------------------------------------
@@ -229,13 +261,16 @@ zvc_status zvc_get_error(void* d_ws, void* stream);
  * Size: 32 + 8 nw + 4 (records + non-zeros), at most 32 + 12 nw + 4 n. */
 #define ZVC_RLE_MAX_WINDOW 4096u    /* words; the paper's 4 KB window is 1024 */
 
-/* Worst-case RLE stream bytes for n words in windows of W (0 on invalid arguments). */
+/* Worst-case RLE stream bytes for n words in windows of W (0 on invalid arguments).
+ * Cites section V.A "Compression Algorithm" (RLE) under this library's record layout. */
 uint64_t zvc_rle_size_bound(uint64_t n, uint32_t window);
 
-/* Workspace bytes for zvc_rle_compress (window sizes and scan totals). */
+/* Workspace bytes for zvc_rle_compress (window sizes and scan totals). Cites section V.A
+ * (RLE) and section VII.A "Compression Efficiency" (per 4 KB window). */
 uint64_t zvc_rle_workspace_size(uint64_t n, uint32_t window);
 
-/* RLE-compress n words at d_in (4-byte aligned) into d_out (8-byte aligned, out_cap >=
+/* RLE-compress (section V.A "Compression Algorithm": runs of zeros and of non-zeros;
+ * section VII.A: per window) n words at d_in (4-byte aligned) into d_out (8-byte aligned, out_cap >=
  * zvc_rle_size_bound), writing the stream's byte count to *d_out_size (device, 8-byte
  * aligned). Reads the input twice (window sizes, then the records); asynchronous. */
 zvc_status zvc_rle_compress(const void* d_in, uint64_t n, uint32_t window, void* d_out,
@@ -243,16 +278,18 @@ zvc_status zvc_rle_compress(const void* d_in, uint64_t n, uint32_t window, void*
                             void* stream);
 
 /* Decompress the RLE stream of in_bytes bytes at d_in (8-byte aligned) into n words at
- * d_out. Host-visible size errors return ZVC_ERR_CORRUPT; every other check (header,
+ * d_out (the inverse of section V.A's RLE). Host-visible size errors return ZVC_ERR_CORRUPT; every other check (header,
  * window offsets, records covering each window exactly) latches ZVC_ERR_CORRUPT in d_ws
  * (at least 256 bytes; read it with zvc_get_error), with no access outside the buffers. */
 zvc_status zvc_rle_decompress(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,
                               uint32_t window, void* d_ws, uint64_t ws_bytes, void* stream);
 
-/* The cudaError_t value behind the most recent ZVC_ERR_CUDA on this thread. */
+/* The cudaError_t value behind the most recent ZVC_ERR_CUDA on this thread. The paper
+ * has no counterpart: a library convenience. */
 int zvc_last_cuda_error(void);
 
-/* A static, human-readable name for a zvc_status. */
+/* A static, human-readable name for a zvc_status. The paper has no counterpart: a
+ * library convenience. */
 const char* zvc_status_string(zvc_status s);
 
 #ifdef __cplusplus

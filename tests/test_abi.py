@@ -102,3 +102,18 @@ def test_offload_hooks_reject_an_unknown_placement():
     from activation_sparsity_compression_gb300.offload import ActivationOffload
     with pytest.raises(ValueError):
         ActivationOffload(where="disk")
+
+
+def test_every_declaration_cites_its_passage():
+    """The comment above each function declared in include/zvc.h names the paper's
+    section it follows, or says that the paper has no counterpart."""
+    text = open(zvc.HEADER_PATH).read()
+    names = zvc.header_functions()
+    for name in names:
+        m = re.search(r"^(?:const\s+)?[a-z_0-9]+\s*\*?\s*" + name + r"\s*\(", text, re.M)
+        assert m, name
+        # the last comment block that opens a line above the declaration (a trailing
+        # comment on a #define line is not one)
+        blocks = [c for c in re.finditer(r"^/\*.*?\*/", text, re.M | re.S) if c.end() <= m.start()]
+        comment = blocks[-1].group(0)
+        assert ("section" in comment) or ("no counterpart" in comment), name

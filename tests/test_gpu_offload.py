@@ -113,3 +113,64 @@ def test_offload_rejects_a_host_buffer_off_8_byte_alignment():
     st, _ = zvc.zvc_offload(x.data_ptr(), n, C, h.data_ptr() + 4, cap, ws.data_ptr(), ws.numel(),
                             sh())
     assert st == zvc.ZVC_ERR_INVALID_ARG
+
+
+def test_offload_and_prefetch_from_two_threads_at_once():
+    """An offload on one thread (its own stream and workspace) and prefetches of another
+    tensor on a second thread run at the same time: the library's per-device lock is
+    held only around its copy-stream enqueues, never while a call waits for a kernel.
+    Every host batch equals the oracle's, every restored tensor is bit-exact."""
+    import threading
+
+    ensure_lib()
+    C = 4096
+    n_a, n_b = 70_000_011, 40_000_003  # 3 and 2 offload segments
+    xa = workloads.odd_case(n_a, device="cuda", density=0.35)[0]
+    xb = workloads.odd_case(n_b, device="cuda", density=0.55)[0]
+    hb, size_b, ws_b = _offload(xb, C)
+    cap_a = zvc.zvc_offload_host_bound(n_a, C)
+    ha = [torch.empty(cap_a, dtype=torch.uint8, pin_memory=True) for _ in range(3)]
+    ws_a = zvc.new_workspace(zvc.zvc_offload_workspace_size(n_a, C))
+    ys = [torch.full((n_b,), -1, dtype=torch.int32, device="cuda") for _ in range(3)]
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    results = {}
+    start = threading.Barrier(2)
+
+    def offloader():
+        torch.cuda.set_device(0)
+        start.wait()
+        out = []
+        for h in ha:
+            out.append(zvc.zvc_offload(xa.data_ptr(), n_a, C, h.data_ptr(), cap_a,
+                                       ws_a.data_ptr(), ws_a.numel(), sa.cuda_stream))
+        results["a"] = out
+
+    def prefetcher():
+        torch.cuda.set_device(0)
+        start.wait()
+        results["b"] = [zvc.zvc_prefetch(hb.data_ptr(), size_b, y.data_ptr(), n_b, C,
+                                         ws_b.data_ptr(), ws_b.numel(), sb.cuda_stream)
+                        for y in ys]
+
+    threads = [threading.Thread(target=offloader), threading.Thread(target=prefetcher)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert zvc.zvc_offload_join(sa.cuda_stream) == zvc.ZVC_OK
+    torch.cuda.synchronize()
+    assert zvc.zvc_get_error(ws_a.data_ptr(), sh()) == zvc.ZVC_OK
+    assert zvc.zvc_get_error(ws_b.data_ptr(), sh()) == zvc.ZVC_OK
+    assert all(st == zvc.ZVC_OK for st, _ in results["a"])
+    assert all(st == zvc.ZVC_OK for st in results["b"])
+    seg = zvc.zvc_offload_segment_elems(n_a, C)
+    w = words_of(xa)
+    ref = oracle.encode_batch([w[k:k + seg] for k in range(0, n_a, seg)], C)
+    for h, (_, size) in zip(ha, results["a"]):
+        assert size == ref.size
+        assert np.array_equal(h[:size].numpy(), ref)
+    for y in ys:
+        assert torch.equal(y, xb.view(torch.int32))
