@@ -44,20 +44,39 @@ def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(tmp_path, m
     assert bench.traffic_per_launch("decompress_kernel", 1e6) is None
 
 
-def test_write_traffic_checks_the_launch_count(tmp_path, monkeypatch):
+def test_write_traffic_records_bytes_per_word_of_one_launch_each(tmp_path, monkeypatch):
     pytest.importorskip("torch")
+    import math
+
+    import workloads
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "traffic.json"))
-    L = bench.launches_per_step(4096)
-    assert L == 6  # AlexNet layer 0 takes two 32 Mi-word segments, the others one each
-    ok = [("1", "1", "Mbyte")] * L
-    c = _csv(tmp_path / "c.csv", ok)
-    d = _csv(tmp_path / "d.csv", ok)
-    assert bench.write_traffic([c, d], 4096) == 0
+    words = sum(math.prod(s.shape) for s in workloads.googlenet_specs(16))
+    assert words == 3_020_193_792 // 16  # batch 16 is 1/16 of the batch-256 workload
+    c = _csv(tmp_path / "c.csv", [("3", "1", "Gbyte")])
+    d = _csv(tmp_path / "d.csv", [("1", "3", "Gbyte")])
+    assert bench.write_traffic([c, d], 4096, 16) == 0
     rec = json.loads((tmp_path / "traffic.json").read_text())
+    assert rec["words_per_launch"] == words
     for k in ("compress_kernel", "decompress_kernel"):
-        assert rec["kernels"][k]["launches"] == L
-        assert rec["kernels"][k]["dram_bytes"] == pytest.approx(2e6 * L)
+        assert rec["kernels"][k]["dram_bytes"] == pytest.approx(4e9)
+        assert rec["kernels"][k]["dram_bytes_per_word"] == pytest.approx(4e9 / words)
+        assert rec["kernels"][k]["gpu_time_us"] == pytest.approx(12.5)
         assert rec["kernels"][k]["source_sha256"] == bench.kernel_source_hash(k)
-    short = _csv(tmp_path / "s.csv", ok[:-1])
+    # scaled to a full-size launch by its words
+    assert bench.traffic_per_launch("compress_kernel", 16 * words) == pytest.approx(64e9)
+    two = _csv(tmp_path / "two.csv", [("1", "1", "Mbyte")] * 2)
     with pytest.raises(SystemExit):
-        bench.write_traffic([c, short], 4096)
+        bench.write_traffic([c, two], 4096, 16)
+
+
+def test_host_cpu_reports_cores_and_a_model():
+    cores, model = bench.host_cpu()
+    assert cores >= 1 and isinstance(model, str) and model
+
+
+def test_clock_sampler_falls_back_without_nvml():
+    # no NVIDIA driver here: the NVML sampler is unavailable and nvidia-smi takes over
+    s = bench.clock_sampler(None)
+    assert isinstance(s, (bench.NvmlSampler, bench.ClockSampler))
+    if isinstance(s, bench.NvmlSampler):
+        assert s.available()
