@@ -167,9 +167,10 @@ _rle_lib = None
 
 
 def build_all() -> None:
-    """Compile both oracle libraries (ZVC and RLE)."""
+    """Compile every oracle library (ZVC on 32-bit words, ZVC on 16-bit words, RLE)."""
     build()
     build(_RLE_SRC, _RLE_LIB_PATH)
+    build(_Z16_SRC, _Z16_LIB_PATH)
 
 
 def rle_load(path: str | None = None):
@@ -225,4 +226,79 @@ def rle_decode(stream, n: int, window: int = 1024, lib=None):
     s = np.ascontiguousarray(stream, dtype=np.uint8).reshape(-1)
     y = np.full(max(n, 1), _POISON, dtype=np.uint32)
     r = lib.rleo_decode(_ptr(s, ctypes.c_uint8), s.size, _ptr(y, ctypes.c_uint32), n, window)
+    return int(r), y[:n]
+
+
+# ------------------------------------------------------------------ ZVC on 16-bit words
+# The same rule on bf16 / fp16 activation words (a 32-bit mask per 32 values, then the
+# non-zero 2-byte values); the layout is documented at the top of ``zvc16_oracle.c``. A
+# separate library, so that the 32-bit oracle above stays exactly as pinned.
+_Z16_SRC = os.path.join(_HERE, "zvc16_oracle.c")
+_Z16_LIB_PATH = os.path.join(_BUILD_DIR, "libzvc16_oracle.so")
+_z16_lib = None
+
+
+def z16_load(path: str | None = None):
+    """Load (building first if needed) the 16-bit ZVC oracle library. ``path`` (or the
+    environment variable ZVC16_ORACLE_LIB) loads a specific build, e.g. a mutant."""
+    global _z16_lib
+
+    def declare(lib):
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        lib.zvco16_size_bound.restype = ctypes.c_uint64
+        lib.zvco16_size_bound.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        lib.zvco16_encode.restype = ctypes.c_int64
+        lib.zvco16_encode.argtypes = [u16p, ctypes.c_uint64, ctypes.c_uint32, u8p, ctypes.c_uint64]
+        lib.zvco16_decode.restype = ctypes.c_int
+        lib.zvco16_decode.argtypes = [u8p, ctypes.c_uint64, u16p, ctypes.c_uint64, ctypes.c_uint32]
+        return lib
+
+    path = path or os.environ.get("ZVC16_ORACLE_LIB")
+    if path is not None:
+        return declare(ctypes.CDLL(path))
+    with _lock:
+        if _z16_lib is None:
+            stale = (not os.path.exists(_Z16_LIB_PATH)
+                     or os.path.getmtime(_Z16_LIB_PATH) < os.path.getmtime(_Z16_SRC))
+            if stale:
+                build(_Z16_SRC, _Z16_LIB_PATH)
+            _z16_lib = declare(ctypes.CDLL(_Z16_LIB_PATH))
+    return _z16_lib
+
+
+def _u16_words(x) -> np.ndarray:
+    a = np.ascontiguousarray(x)
+    if a.dtype.itemsize != 2:
+        raise TypeError(f"16-bit ZVC works on 16-bit words, got {a.dtype}")
+    return a.reshape(-1).view(np.uint16)
+
+
+def size_bound16(n: int, chunk_elems: int, lib=None) -> int:
+    lib = lib or z16_load()
+    return int(lib.zvco16_size_bound(n, chunk_elems))
+
+
+def encode16(x, chunk_elems: int = 4096, lib=None) -> np.ndarray:
+    """Encode a 2-byte-per-element array (any shape) into one 16-bit ZVC stream (uint8)."""
+    lib = lib or z16_load()
+    w = _u16_words(x)
+    n = w.size
+    cap = int(lib.zvco16_size_bound(n, chunk_elems))
+    if cap == 0:
+        raise OracleError(ERR_INVALID_ARG)
+    out = np.empty(cap, dtype=np.uint8)
+    r = lib.zvco16_encode(_ptr(w, ctypes.c_uint16), n, chunk_elems, _ptr(out, ctypes.c_uint8), cap)
+    if r < 0:
+        raise OracleError(int(r))
+    return out[:r].copy()
+
+
+def decode16(stream, n: int, chunk_elems: int = 4096, lib=None):
+    """Decode one 16-bit stream. Returns (status, words) with words a uint16 array of n."""
+    lib = lib or z16_load()
+    s = np.ascontiguousarray(stream, dtype=np.uint8).reshape(-1)
+    y = np.full(max(n, 1), 0xA5A5, dtype=np.uint16)  # every word must be written
+    r = lib.zvco16_decode(_ptr(s, ctypes.c_uint8), s.size, _ptr(y, ctypes.c_uint16), n,
+                          chunk_elems)
     return int(r), y[:n]

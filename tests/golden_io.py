@@ -7,8 +7,8 @@ import numpy as np
 GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
-def _parse_words(spec: str, n: int) -> np.ndarray:
-    w = np.zeros(n, dtype=np.uint32)
+def _parse_words(spec: str, n: int, dtype=np.uint32) -> np.ndarray:
+    w = np.zeros(n, dtype=dtype)
     for tok in spec.split():
         i, v = tok.split("=")
         w[int(i)] = int(v, 16)
@@ -44,6 +44,10 @@ def load(name: str, directory: str = GOLDEN_DIR) -> dict:
         return {"name": name, "n": n, "window": int(keys["window"]),
                 "input": _parse_words(keys.get("input", ""), n), "expected": expected}
     c = int(keys["chunk_elems"])
+    if keys.get("word_bytes") == "2":  # a 16-bit ZVC vector
+        n = int(keys["n"])
+        return {"name": name, "n": n, "chunk_elems": c, "word_bytes": 2,
+                "input": _parse_words(keys.get("input", ""), n, np.uint16), "expected": expected}
     if "batch" in keys:
         ns = [int(s) for s in keys["batch"].split(",")]
         inputs = [_parse_words(keys.get(f"input{k}", ""), n) for k, n in enumerate(ns)]
@@ -72,3 +76,14 @@ def all_rle():
 
 def load_rle(name: str) -> dict:
     return load(name, RLE_DIR)
+
+
+Z16_DIR = os.path.join(GOLDEN_DIR, "zvc16")
+
+
+def all_z16():
+    return sorted(f for f in os.listdir(Z16_DIR) if f.endswith(".txt"))
+
+
+def load_z16(name: str) -> dict:
+    return load(name, Z16_DIR)

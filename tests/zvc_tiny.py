@@ -74,3 +74,67 @@ def tiny_encode_batch(list_of_words, chunk_elems):
     offs = list(itertools.accumulate([len(s) for s in streams], initial=head))
     return (struct.pack("<IIQ", 0x4243565A, len(streams), offs[-1])
             + b"".join(struct.pack("<Q", o) for o in offs) + b"".join(streams))
+
+
+# ---- ZVC on 16-bit words: the same rule with 2-byte values (word_bytes 2 in the header)
+def tiny_encode16(words, chunk_elems):
+    words = [int(v) & 0xFFFF for v in words]
+    n = len(words)
+    bodies = []
+    for c0 in range(0, n, chunk_elems):
+        seg = words[c0:c0 + chunk_elems]
+        parts = []
+        for k in range(0, len(seg), 32):
+            win = seg[k:k + 32]
+            mask = 0
+            vals = b""
+            for i, v in enumerate(win):
+                if v:
+                    mask |= 1 << i
+                    vals += struct.pack("<H", v)
+            parts.append(struct.pack("<I", mask) + vals)
+        bodies.append(b"".join(parts))
+    offs = list(itertools.accumulate([len(b) for b in bodies], initial=0))[:-1]
+    payload = b"".join(bodies)
+    head = struct.pack("<IHHIIQQ", 0x3143565A, 1, 2, 32, chunk_elems, n, len(payload))
+    return head + b"".join(struct.pack("<Q", o) for o in offs) + payload
+
+
+def tiny_decode16(stream, n, chunk_elems):
+    """Returns the 16-bit words, or None if the stream is not a valid encoding of n."""
+    stream = bytes(stream)
+    if len(stream) < 32:
+        return None
+    if struct.unpack_from("<IHHIIQ", stream, 0) != (0x3143565A, 1, 2, 32, chunk_elems, n):
+        return None
+    (pay,) = struct.unpack_from("<Q", stream, 24)
+    nc = -(-n // chunk_elems)
+    base = 32 + 8 * nc
+    if len(stream) != base + pay:
+        return None
+    offs = [struct.unpack_from("<Q", stream, 32 + 8 * i)[0] for i in range(nc)] + [pay]
+    out = []
+    for ci in range(nc):
+        pos, end = offs[ci], offs[ci + 1]
+        if (ci == 0 and pos != 0) or not (pos <= end <= pay):
+            return None
+        count = min(chunk_elems, n - ci * chunk_elems)
+        for k in range(0, count, 32):
+            if pos + 4 > end:
+                return None
+            (mask,) = struct.unpack_from("<I", stream, base + pos)
+            pos += 4
+            valid = min(32, count - k)
+            if mask >> valid:
+                return None
+            for i in range(valid):
+                if mask >> i & 1:
+                    if pos + 2 > end:
+                        return None
+                    out.append(struct.unpack_from("<H", stream, base + pos)[0])
+                    pos += 2
+                else:
+                    out.append(0)
+        if pos != end:
+            return None
+    return out
