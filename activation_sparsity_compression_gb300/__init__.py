@@ -51,6 +51,9 @@ _SIGS = {
     "zvc_compress": (_st, [_vp, _u64, _u32, _vp, _u64, _vp, _vp, _u64, _vp]),
     "zvc_decompress": (_st, [_vp, _u64, _vp, _u64, _u32, _vp, _u64, _vp]),
     "zvc_compress_static": (_st, [_vp, _u64, _u32, _vp, _u64, _vp, _vp]),
+    "zvc_size_bound16": (_u64, [_u64, _u32]),
+    "zvc_compress16": (_st, [_vp, _u64, _u32, _vp, _u64, _vp, _vp, _u64, _vp]),
+    "zvc_decompress16": (_st, [_vp, _u64, _vp, _u64, _u32, _vp, _u64, _vp]),
     "zvc_compress_batched": (_st, [ctypes.POINTER(_vp), ctypes.POINTER(_u64), _u32, _u32, _vp,
                                    _u64, _vp, _vp, _u64, _vp]),
     "zvc_decompress_batched": (_st, [_vp, _u64, ctypes.POINTER(_vp), ctypes.POINTER(_u64), _u32,
@@ -149,6 +152,19 @@ def zvc_compress_static(d_in, n, chunk_elems, d_out, out_cap, d_out_size, stream
 def zvc_compress_static_get_error(stream):
     """Status latched by zvc_compress_static on this device since the last read; clears it."""
     return int(lib().zvc_compress_static_get_error(stream))
+
+
+def zvc_size_bound16(n, chunk_elems):
+    return int(lib().zvc_size_bound16(n, chunk_elems))
+
+
+def zvc_compress16(d_in, n, chunk_elems, d_out, out_cap, d_out_size, d_ws, ws_bytes, stream):
+    return lib().zvc_compress16(d_in, n, chunk_elems, d_out, out_cap, d_out_size, d_ws, ws_bytes,
+                                stream)
+
+
+def zvc_decompress16(d_in, in_bytes, d_out, n, chunk_elems, d_ws, ws_bytes, stream):
+    return lib().zvc_decompress16(d_in, in_bytes, d_out, n, chunk_elems, d_ws, ws_bytes, stream)
 
 
 def zvc_decompress(d_in, in_bytes, d_out, n, chunk_elems, d_ws, ws_bytes, stream):

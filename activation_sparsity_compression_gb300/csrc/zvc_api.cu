@@ -23,8 +23,8 @@ bool chunk_ok(uint32_t c) { return c != 0 && c % kWindow == 0 && c <= ZVC_MAX_CH
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-uint64_t stream_bound(uint64_t n, uint32_t c) {
-  return 32 + 8 * ceil_div_u64(n, c) + 4 * ceil_div_u64(n, kWindow) + 4 * n;
+uint64_t stream_bound(uint64_t n, uint32_t c, uint32_t word_bytes = 4) {
+  return 32 + 8 * ceil_div_u64(n, c) + 4 * ceil_div_u64(n, kWindow) + word_bytes * n;
 }
 
 // Smallest valid stream for n words: every mask zero.
@@ -288,6 +288,42 @@ zvc_status zvc_compress(const void* d_in, uint64_t n, uint32_t chunk_elems, void
   return launch_compress(&t, 1, false, chunk_elems, static_cast<uint32_t*>(d_out), out_cap / 4,
                          d_out_size, static_cast<uint8_t*>(d_ws), kDefaultWaitLimitNs,
                          static_cast<cudaStream_t>(stream));
+}
+
+uint64_t zvc_size_bound16(uint64_t n, uint32_t chunk_elems) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems) return 0;
+  return stream_bound(n, chunk_elems, 2);
+}
+
+zvc_status zvc_compress16(const void* d_in, uint64_t n, uint32_t chunk_elems, void* d_out,
+                          uint64_t out_cap, uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
+                          void* stream) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems || d_out == nullptr || d_ws == nullptr ||
+      (n > 0 && d_in == nullptr) || !aligned(d_in, 2) || !aligned(d_out, 4) ||
+      !aligned(d_ws, ZVC_WORKSPACE_ALIGN) || !aligned(d_out_size, 8))
+    return ZVC_ERR_INVALID_ARG;
+  if (out_cap < stream_bound(n, chunk_elems, 2) || ws_bytes < zvc_workspace_size(n, chunk_elems))
+    return ZVC_ERR_BUFFER_TOO_SMALL;
+  return launch_compress16(static_cast<const uint16_t*>(d_in), n, chunk_elems,
+                           static_cast<uint16_t*>(d_out), out_cap / 2, d_out_size,
+                           static_cast<uint8_t*>(d_ws), kDefaultWaitLimitNs,
+                           static_cast<cudaStream_t>(stream));
+}
+
+zvc_status zvc_decompress16(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,
+                            uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!chunk_ok(chunk_elems) || n > kMaxElems || d_in == nullptr || d_ws == nullptr ||
+      (n > 0 && d_out == nullptr) || !aligned(d_in, 4) || !aligned(d_out, 2) ||
+      !aligned(d_ws, ZVC_WORKSPACE_ALIGN))
+    return ZVC_ERR_INVALID_ARG;
+  if (ws_bytes < kControlBytes) return ZVC_ERR_BUFFER_TOO_SMALL;
+  // sizes no valid stream of n 16-bit words can have
+  if (in_bytes % 2 != 0 || in_bytes < stream_floor(n, chunk_elems) ||
+      in_bytes > stream_bound(n, chunk_elems, 2))
+    return ZVC_ERR_CORRUPT;
+  return launch_decompress16(static_cast<const uint32_t*>(d_in), in_bytes,
+                             static_cast<uint16_t*>(d_out), n, chunk_elems,
+                             static_cast<uint8_t*>(d_ws), static_cast<cudaStream_t>(stream));
 }
 
 zvc_status zvc_decompress(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,

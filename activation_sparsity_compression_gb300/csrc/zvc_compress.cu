@@ -33,24 +33,31 @@
 namespace zvc {
 namespace {
 
-template <int MAXT>
+// WB is the word size in bytes: 4 (any 32-bit type) or 2 (bf16 / fp16). Positions in the
+// stream are counted in units of one word: a mask is 4 / WB units.
+template <int WB> struct WordOf;
+template <> struct WordOf<4> { using T = uint32_t; };
+template <> struct WordOf<2> { using T = uint16_t; };
+
+template <int MAXT, int WB>
 struct CompressArgs {
-  uint32_t* out;
-  uint64_t out_words;
+  using Word = typename WordOf<WB>::T;
+  Word* out;
+  uint64_t out_words;  // units of WB bytes
   uint64_t* out_size;
   uint8_t* ws;
   uint64_t total_tiles;
   uint64_t wait_limit_ns;
   uint64_t epoch;          // tags this launch's entries in the workspace
-  uint64_t hdr_words_end;  // batch prefix + every stream's header and table, in words
+  uint64_t hdr_words_end;  // batch prefix + every stream's header and table, in units
   uint32_t chunk_elems;
   uint32_t T;
   uint32_t batched;
   uint32_t inner_chunks;  // 1 when chunks can start inside a tile (C not a multiple of 4096)
-  const uint32_t* in[MAXT];
+  const Word* in[MAXT];
   uint64_t n[MAXT];
   uint64_t tile_begin[MAXT + 1];  // first tile of tensor i; tile_begin[T] = total_tiles
-  uint64_t hdr_before[MAXT];      // header/table words (and batch prefix) before stream i
+  uint64_t hdr_before[MAXT];      // header/table units (and batch prefix) before stream i
   uint64_t payload_base[MAXT];    // hdr_before + this stream's header and table
 };
 
@@ -69,7 +76,9 @@ __device__ __forceinline__ void put_u64_words(uint32_t* p, uint64_t v) {
 // The store warp that empties a slot starts its refill, so no barrier marks it empty.
 constexpr int kSlots = 12;
 constexpr uint32_t kInOffset = kTileWindows;                 // input lands 128 words in
-constexpr uint32_t kSlotWords = kInOffset + kTileElems;      // 4224: a dense tile's packed size
+// Slot words: the input lands 512 bytes in; a dense tile packs into 512 + 4096 WB bytes
+// (4224 words for WB = 4, 2176 for WB = 2), which is the slot.
+constexpr uint32_t slot_words(int wb) { return kInOffset + kTileElems * (uint32_t)wb / 4u; }
 constexpr int kTeamWarps = 8;                                // a pack team: 16 windows per warp
 constexpr int kTeams = 2;                                    // warps 0..7 and 8..15
 constexpr uint32_t kWinPerWarp = kTileWindows / kTeamWarps;  // 32
@@ -97,8 +106,9 @@ struct SlotInfo {
   uint32_t pad;
 };
 
+template <int WB>
 struct __align__(16) CompressShared {
-  uint32_t slot[kSlots][kSlotWords];
+  uint32_t slot[kSlots][slot_words(WB)];
   uint32_t woff[kSlots][kTileWindows];  // window offsets, kept only when chunks start inside tiles
   SlotInfo info[kSlots];
   uint32_t team_tot[kTeams][2][kTeamWarps];  // pack warps' payload words, double-buffered
@@ -109,10 +119,10 @@ struct __align__(16) CompressShared {
   uint64_t pbuf[ZVC_MAX_BATCH + 1];  // stream starts, for the headers
 };
 
-static_assert(sizeof(CompressShared) <= 227 * 1024, "one CTA per SM must fit");
+static_assert(sizeof(CompressShared<4>) <= 227 * 1024, "one CTA per SM must fit");
 
-template <int MAXT>
-__device__ __forceinline__ uint32_t tensor_of_tile(const CompressArgs<MAXT>& a, uint64_t t) {
+template <int MAXT, int WB>
+__device__ __forceinline__ uint32_t tensor_of_tile(const CompressArgs<MAXT, WB>& a, uint64_t t) {
   uint32_t lo = 0;
   if (MAXT > 1) {
     uint32_t hi = a.T;
@@ -127,14 +137,14 @@ __device__ __forceinline__ uint32_t tensor_of_tile(const CompressArgs<MAXT>& a, 
 // Starts bringing tile t into slot s (one thread). Tiles that are not whole 16-byte-aligned
 // 16 KB blocks (a tensor's ragged last tile, or a tensor whose base is not 16-byte aligned)
 // are marked direct: the pack warp reads them from global memory.
-template <int MAXT>
-__device__ __forceinline__ void fill_slot(const CompressArgs<MAXT>& a, CompressShared& sm, int s,
+template <int MAXT, int WB>
+__device__ __forceinline__ void fill_slot(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& sm, int s,
                                           unsigned long long t) {
   if (t >= a.total_tiles) return;
   const uint32_t ti = tensor_of_tile(a, t);
   const uint64_t lt = t - a.tile_begin[ti];
   const uint64_t e0 = lt * kTileElems;
-  const uint32_t* src = a.in[ti] + e0;
+  const typename CompressArgs<MAXT, WB>::Word* src = a.in[ti] + e0;
   const uint64_t left = a.n[ti] - e0;
   const bool whole = left >= kTileElems && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
   SlotInfo& f = sm.info[s];
@@ -144,8 +154,8 @@ __device__ __forceinline__ void fill_slot(const CompressArgs<MAXT>& a, CompressS
   f.direct = whole ? 0u : 1u;
   if (whole) {
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&sm.full[s], kTileElems * 4);
-    bulk_g2s(&sm.slot[s][kInOffset], src, kTileElems * 4, &sm.full[s]);
+    mbar_arrive_expect_tx(&sm.full[s], kTileElems * WB);
+    bulk_g2s(&sm.slot[s][kInOffset], src, kTileElems * WB, &sm.full[s]);
   } else {
     mbar_arrive(&sm.full[s]);
   }
@@ -156,8 +166,8 @@ __device__ __forceinline__ void fill_slot(const CompressArgs<MAXT>& a, CompressS
 // which case a failure upstream has been latched already.
 // A tensor's start in the payload, published by its first tile in this launch (bounded
 // wait); false if that tile gave up or the wait ran out.
-template <int MAXT>
-__device__ bool wait_tensor_start(const CompressArgs<MAXT>& a, const TensorStart* ts, Control* ctl,
+template <int MAXT, int WB>
+__device__ bool wait_tensor_start(const CompressArgs<MAXT, WB>& a, const TensorStart* ts, Control* ctl,
                                   uint64_t info, uint64_t* value) {
   WaitClock clock;
   while (true) {
@@ -175,8 +185,8 @@ __device__ bool wait_tensor_start(const CompressArgs<MAXT>& a, const TensorStart
   return false;
 }
 
-template <int MAXT>
-__device__ void finalize_warp(const CompressArgs<MAXT>& a, uint64_t total_payload, bool failed,
+template <int MAXT, int WB>
+__device__ void finalize_warp(const CompressArgs<MAXT, WB>& a, uint64_t total_payload, bool failed,
                               const TensorStart* tstart, Control* ctl, uint64_t* pbuf,
                               uint32_t lane) {
   int bad = failed;
@@ -202,22 +212,24 @@ __device__ void finalize_warp(const CompressArgs<MAXT>& a, uint64_t total_payloa
   if (bad) return;
   for (uint32_t i = lane; i < a.T; i += 32) {
     const uint64_t s0 = a.hdr_before[i] + pbuf[i];
-    uint32_t* h = a.out + s0;
+    uint32_t* h = reinterpret_cast<uint32_t*>(a.out + s0);  // 4-byte aligned: see launch_t
     h[0] = kStreamMagic;
-    h[1] = kVersionWordBytes;
+    h[1] = 1u | ((uint32_t)WB << 16);  // u16 version 1, u16 word_bytes
     h[2] = kWindow;
     h[3] = a.chunk_elems;
     put_u64_words(h + 4, a.n[i]);
-    put_u64_words(h + 6, 4 * (pbuf[i + 1] - pbuf[i]));
-    if (a.batched) put_u64_words(a.out + kBatchHeaderWords + 2 * i, 4 * s0);
+    put_u64_words(h + 6, WB * (pbuf[i + 1] - pbuf[i]));
+    if (a.batched)
+      put_u64_words(reinterpret_cast<uint32_t*>(a.out) + kBatchHeaderWords + 2 * i, WB * s0);
   }
   if (lane == 0) {
-    const uint64_t total_bytes = 4 * (a.hdr_words_end + total_payload);
+    const uint64_t total_bytes = WB * (a.hdr_words_end + total_payload);
     if (a.batched) {
-      a.out[0] = kBatchMagic;
-      a.out[1] = a.T;
-      put_u64_words(a.out + 2, total_bytes);
-      put_u64_words(a.out + kBatchHeaderWords + 2 * a.T, total_bytes);
+      uint32_t* b = reinterpret_cast<uint32_t*>(a.out);
+      b[0] = kBatchMagic;
+      b[1] = a.T;
+      put_u64_words(b + 2, total_bytes);
+      put_u64_words(b + kBatchHeaderWords + 2 * a.T, total_bytes);
     }
     if (a.out_size) *a.out_size = total_bytes;
   }
@@ -237,46 +249,78 @@ __device__ __forceinline__ bool team_any(uint32_t team, bool c) {
   return r != 0;
 }
 
-// Writes one window (this lane's word v, the window's mask m) at word pos of the slot and
-// returns the position after it.
+// Writes one window (this lane's word v, the window's mask m) at unit pos of the slot and
+// returns the position after it. A mask is 4 / WB units; with WB = 2 lanes 0 and 1 store
+// its two halves, since it need not start on a 4-byte boundary.
+template <int WB>
 __device__ __forceinline__ uint32_t pack_window(uint32_t* slot, uint32_t pos, uint32_t v,
                                                 uint32_t m, uint32_t lane, uint32_t lane_below) {
-  if (v != 0u) slot[pos + 1u + __popc(m & lane_below)] = v;
-  if (lane == 0) slot[pos] = m;
-  return pos + 1u + __popc(m);
+  using Word = typename WordOf<WB>::T;
+  constexpr uint32_t mu = 4u / WB;
+  Word* u = reinterpret_cast<Word*>(slot);
+  if (v != 0u) u[pos + mu + __popc(m & lane_below)] = (Word)v;
+  if (WB == 4) {
+    if (lane == 0) u[pos] = (Word)m;
+  } else if (lane < 2) {
+    u[pos + lane] = (Word)(m >> (16u * lane));
+  }
+  return pos + mu + __popc(m);
 }
 
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// Writes this warp's windows of a whole tile into the slot from word pos on: per window one
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
+}
+
+// One packed word (WB bytes) at a shared-memory byte address.
+template <int WB>
+__device__ __forceinline__ void st_shared_word(uint32_t addr, uint32_t v) {
+  if (WB == 4) st_shared_u32(addr, v);
+  else st_shared_u16(addr, v);
+}
+
+// A window's mask at a shared-memory byte address: lane 0 stores it whole (WB = 4); with
+// WB = 2 it may sit on a 2-byte boundary, and lanes 0 and 1 store its halves.
+template <int WB>
+__device__ __forceinline__ void st_shared_mask(uint32_t addr, uint32_t m, uint32_t lane) {
+  if (WB == 4) {
+    if (lane == 0) st_shared_u32(addr, m);
+  } else if (lane < 2) {
+    st_shared_u16(addr + 2u * lane, m >> (16u * lane));
+  }
+}
+
+// Writes this warp's windows of a whole tile into the slot from unit pos on: per window one
 // store of the non-zero words, each at its rank among the window's set bits, and one of the
-// mask by lane 0. Addresses are 32-bit shared-memory byte addresses, and each window's own
-// mask word offset (4j bytes) is an immediate of its stores, so the running address only
-// adds the non-zero words of the windows before. With SKIP a warp-uniform branch passes
+// mask. Addresses are 32-bit shared-memory byte addresses, and each window's own mask
+// bytes (4j for window j) are an immediate of its stores, so the running address only adds
+// the non-zero words of the windows before. With SKIP a warp-uniform branch passes
 // over an empty window, which is its mask alone: fewer instructions where most windows are
 // empty, and (measured) faster where none is; between those the plain loop wins. With WOFF
 // lane 0 also records each window's word offset, for chunks that start inside the tile.
-template <bool SKIP, bool WOFF>
+template <int WB, bool SKIP, bool WOFF>
 __device__ __forceinline__ void pack_whole(uint32_t slot_addr, uint32_t pos,
                                            const uint32_t (&v)[kWinPerWarp],
                                            const uint32_t (&m)[kWinPerWarp], uint32_t lane,
                                            uint32_t lane_below, uint32_t* woff) {
-  uint32_t acc = slot_addr + 4u * pos;
+  constexpr uint32_t B = (uint32_t)WB;
+  uint32_t acc = slot_addr + B * pos;
 #pragma unroll
   for (uint32_t j = 0; j < kWinPerWarp; ++j) {
-    if (WOFF && lane == 0) woff[j] = ((acc - slot_addr) >> 2) + j;
+    if (WOFF && lane == 0) woff[j] = (acc - slot_addr) / B + (4u / B) * j;
     if (SKIP) {
-      if (lane == 0) st_shared_u32(acc + 4u * j, m[j]);
+      st_shared_mask<WB>(acc + 4u * j, m[j], lane);
       if (m[j] != 0u) {
-        if (v[j] != 0u) st_shared_u32(acc + 4u * __popc(m[j] & lane_below) + 4u * j + 4u, v[j]);
-        acc += 4u * __popc(m[j]);
+        if (v[j] != 0u) st_shared_word<WB>(acc + B * __popc(m[j] & lane_below) + 4u * j + 4u, v[j]);
+        acc += B * __popc(m[j]);
       }
     } else {
-      if (v[j] != 0u) st_shared_u32(acc + 4u * __popc(m[j] & lane_below) + 4u * j + 4u, v[j]);
-      if (lane == 0) st_shared_u32(acc + 4u * j, m[j]);
-      acc += 4u * __popc(m[j]);
+      if (v[j] != 0u) st_shared_word<WB>(acc + B * __popc(m[j] & lane_below) + 4u * j + 4u, v[j]);
+      st_shared_mask<WB>(acc + 4u * j, m[j], lane);
+      acc += B * __popc(m[j]);
     }
   }
 }
@@ -288,8 +332,8 @@ __device__ __forceinline__ void pack_whole(uint32_t slot_addr, uint32_t pos,
 constexpr uint32_t kSkipBelow = 16;
 constexpr uint32_t kSkipAbove = 320;
 
-template <int MAXT>
-__device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint64_t* status,
+template <int MAXT, int WB>
+__device__ void pack_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& sm, uint64_t* status,
                           Control* ctl, uint32_t team, uint32_t q, uint32_t lane) {
   const unsigned long long G = gridDim.x;
   const uint32_t lane_below = (1u << lane) - 1u;
@@ -311,10 +355,12 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
 #pragma unroll
       for (uint32_t j = 0; j < kWinPerWarp; ++j) v[j] = 0u;
     } else if (!f.direct) {
+      const typename CompressArgs<MAXT, WB>::Word* in =
+          reinterpret_cast<const typename CompressArgs<MAXT, WB>::Word*>(slot + kInOffset);
 #pragma unroll
-      for (uint32_t j = 0; j < kWinPerWarp; ++j) v[j] = slot[kInOffset + (w0 + j) * kWindow + lane];
+      for (uint32_t j = 0; j < kWinPerWarp; ++j) v[j] = in[(w0 + j) * kWindow + lane];
     } else {  // read from global memory; a ragged tile has fewer windows
-      const uint32_t* src = a.in[f.ti] + f.lt * kTileElems;
+      const typename CompressArgs<MAXT, WB>::Word* src = a.in[f.ti] + f.lt * kTileElems;
       const uint32_t valid = f.valid;
       nwin = (valid + kWindow - 1) / kWindow;
 #pragma unroll
@@ -334,7 +380,7 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
       nz += v[j] != 0u ? 1u : 0u;
     }
     const uint32_t held = nwin > w0 ? min(nwin - w0, kWinPerWarp) : 0u;
-    const uint32_t tot = held + __reduce_add_sync(0xffffffffu, nz);
+    const uint32_t tot = held * (4u / WB) + __reduce_add_sync(0xffffffffu, nz);
     uint32_t* tt = sm.team_tot[team][round & 1u];
     if (lane == 0) tt[q] = tot;
     // every word of the tile is read and every warp total is in; a late warp gives up the
@@ -354,22 +400,22 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
     }
     // write back, packed (a store of the non-zero words and one of the mask per window,
     // which costs fewer instructions than folding the mask into the lanes holding a zero)
-    const uint32_t nzw = tot - held;  // the warp's non-zero words
+    const uint32_t nzw = tot - held * (4u / WB);  // the warp's non-zero words
     const uint32_t sa = smem_addr(slot);
     uint32_t* woff = sm.woff[s] + w0;
     if (nwin == kTileWindows && !keep_woff && (nzw <= kSkipBelow || nzw >= kSkipAbove)) {
-      pack_whole<true, false>(sa, pos, v, m, lane, lane_below, woff);
+      pack_whole<WB, true, false>(sa, pos, v, m, lane, lane_below, woff);
     } else if (nwin == kTileWindows && !keep_woff) {
-      pack_whole<false, false>(sa, pos, v, m, lane, lane_below, woff);
+      pack_whole<WB, false, false>(sa, pos, v, m, lane, lane_below, woff);
     } else if (nwin == kTileWindows) {  // chunks start inside tiles: window offsets are kept
       // one loop only: every unrolled copy of the loop in this kernel slows all of them
-      pack_whole<false, true>(sa, pos, v, m, lane, lane_below, woff);
+      pack_whole<WB, false, true>(sa, pos, v, m, lane, lane_below, woff);
     } else {  // a ragged tile
 #pragma unroll
       for (uint32_t j = 0; j < kWinPerWarp; ++j) {
         if (w0 + j < nwin) {
           if (keep_woff && lane == 0) sm.woff[s][w0 + j] = pos;
-          pos = pack_window(slot, pos, v[j], m[j], lane, lane_below);
+          pos = pack_window<WB>(slot, pos, v[j], m[j], lane, lane_below);
         }
       }
     }
@@ -384,8 +430,8 @@ __device__ void pack_role(const CompressArgs<MAXT>& a, CompressShared& sm, uint6
 // ahead: no settle waits for another CTA's settle. Two warps take alternate tiles; each
 // sums its window on its own and then adds the previous tile's inclusive prefix, handed
 // over through shared memory.
-template <int MAXT>
-__device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, const uint64_t* status,
+template <int MAXT, int WB>
+__device__ void settle_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& sm, const uint64_t* status,
                             TensorStart* tstart, Control* ctl, uint32_t k, uint32_t lane) {
   const unsigned long long G = gridDim.x;
   uint64_t lb[kLookbackWidth];
@@ -454,9 +500,52 @@ __device__ void settle_role(const CompressArgs<MAXT>& a, CompressShared& sm, con
   }
 }
 
+// ---- the packed tile's copy for WB = 2: units up to the destination's first 16-byte
+// boundary one per lane, then 16-byte stores, each put together from the two aligned
+// 16-byte groups of the slot it straddles (the slot-side byte phase is twice the head), then
+// the last units one per lane. The second group may reach up to 14 bytes past the packed
+// tile: still inside the shared-memory block, and those bytes are not used.
+template <int PH>  // slot-side byte phase: even, 0..14
+__device__ __forceinline__ uint4 take16(const uint4& x, const uint4& y) {
+  const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+  constexpr int q = PH / 4;
+  if (PH % 4 == 0) return make_uint4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+  return make_uint4(__funnelshift_r(w[q], w[q + 1], 16), __funnelshift_r(w[q + 1], w[q + 2], 16),
+                    __funnelshift_r(w[q + 2], w[q + 3], 16), __funnelshift_r(w[q + 3], w[q + 4], 16));
+}
+
+template <int PH>
+__device__ __forceinline__ void copy_body16(uint4* gv, const uint4* sv, uint32_t nv, uint32_t lane) {
+#pragma unroll 4
+  for (uint32_t q = lane; q < nv; q += 32) gv[q] = PH == 0 ? sv[q] : take16<PH>(sv[q], sv[q + 1]);
+}
+
+__device__ __forceinline__ void copy_out16(uint16_t* g, const uint32_t* src, uint32_t units,
+                                           uint32_t lane) {
+  const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+  const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(g) & 15u);  // even
+  const uint32_t head = min(units, ((16u - mis) & 15u) >> 1);
+  if (lane < head) g[lane] = s16[lane];
+  const uint32_t nv = (units - head) >> 3;
+  uint4* gv = reinterpret_cast<uint4*>(g + head);
+  const uint4* sv = reinterpret_cast<const uint4*>(src);
+  switch (head) {
+    case 0: copy_body16<0>(gv, sv, nv, lane); break;
+    case 1: copy_body16<2>(gv, sv, nv, lane); break;
+    case 2: copy_body16<4>(gv, sv, nv, lane); break;
+    case 3: copy_body16<6>(gv, sv, nv, lane); break;
+    case 4: copy_body16<8>(gv, sv, nv, lane); break;
+    case 5: copy_body16<10>(gv, sv, nv, lane); break;
+    case 6: copy_body16<12>(gv, sv, nv, lane); break;
+    default: copy_body16<14>(gv, sv, nv, lane); break;
+  }
+  const uint32_t done = head + 8u * nv;
+  if (lane < units - done) g[done + lane] = s16[done + lane];
+}
+
 // ---- store warps: copy the packed tile out, write its chunk table entries, refill the slot
-template <int MAXT>
-__device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Control* ctl,
+template <int MAXT, int WB>
+__device__ void store_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& sm, Control* ctl,
                            uint32_t k, uint32_t lane) {
   const unsigned long long G = gridDim.x;
   const uint32_t wpc = a.chunk_elems / kWindow;
@@ -470,9 +559,11 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
     }
     const SlotInfo& f = sm.info[s];
     const uint32_t* src = sm.slot[s];
-    if (f.ok) {
+    if (f.ok && WB == 2) {
+      copy_out16(reinterpret_cast<uint16_t*>(a.out + f.dst), src, f.agg, lane);
+    } else if (f.ok) {
       const uint32_t agg = f.agg;
-      uint32_t* g = a.out + f.dst;
+      uint32_t* g = reinterpret_cast<uint32_t*>(a.out + f.dst);
       // words up to the first 16-byte boundary of the destination, then 16-byte stores;
       // where the slot side is not 16-byte aligned, every lane reads the two aligned 16-byte
       // groups its four words straddle (conflict-free, unlike four strided 4-byte loads) and
@@ -507,19 +598,23 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
       }
       const uint32_t done = head + 4 * nv;
       if (lane < agg - done) g[done + lane] = src[done + lane];
-      // chunk table entries of the chunks that start in this tile
-      uint32_t* table = a.out + a.hdr_before[f.ti] + f.pstart + kStreamHeaderWords;
+    }
+    if (f.ok) {
+      // chunk table entries of the chunks that start in this tile (the stream, its header
+      // and its table start on 4-byte boundaries: see launch_t)
+      uint32_t* table = reinterpret_cast<uint32_t*>(a.out + a.hdr_before[f.ti] + f.pstart) +
+                        kStreamHeaderWords;
       const uint64_t in_stream = f.excl - f.pstart;  // payload words of the stream before the tile
       const uint64_t w_first = f.lt * kTileWindows;
       if (!a.inner_chunks) {  // chunks are whole tiles: at most window 0 starts one
         if (lane == 0 && w_first % wpc == 0)
-          put_u64_words(table + 2 * (w_first / wpc), 4 * in_stream);
+          put_u64_words(table + 2 * (w_first / wpc), WB * in_stream);
       } else {  // the first chunk starting in the tile, then one every wpc windows
         const uint32_t nwin = (f.valid + kWindow - 1) / kWindow;
         const uint64_t c0 = (w_first + wpc - 1) / wpc;
         const uint32_t first = (uint32_t)(c0 * wpc - w_first);
         for (uint32_t w = first + lane * wpc, c = lane; w < nwin; w += 32 * wpc, c += 32)
-          put_u64_words(table + 2 * (c0 + c), 4 * (in_stream + sm.woff[s][w]));
+          put_u64_words(table + 2 * (c0 + c), WB * (in_stream + sm.woff[s][w]));
       }
     }
     // the slot is read; it takes tile i + kSlots next
@@ -529,11 +624,11 @@ __device__ void store_role(const CompressArgs<MAXT>& a, CompressShared& sm, Cont
   }
 }
 
-template <int MAXT>
+template <int MAXT, int WB>
 __global__ void __launch_bounds__(kRoleThreads, 1)
-    compress_kernel(const __grid_constant__ CompressArgs<MAXT> a) {
+    compress_kernel(const __grid_constant__ CompressArgs<MAXT, WB> a) {
   extern __shared__ __align__(16) uint8_t dsmem[];
-  CompressShared& sm = *reinterpret_cast<CompressShared*>(dsmem);
+  CompressShared<WB>& sm = *reinterpret_cast<CompressShared<WB>*>(dsmem);
   Control* ctl = reinterpret_cast<Control*>(a.ws);
   // per tile: its aggregate, tagged with this launch's epoch; then the tensor starts
   uint64_t* status = reinterpret_cast<uint64_t*>(a.ws + kStatusOffset);
@@ -599,13 +694,19 @@ uint64_t next_epoch() {
   return g_epoch.fetch_add(1) + 1;
 }
 
-template <int MAXT>
-zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, uint32_t* out,
-                    uint64_t out_words, uint64_t* out_size, uint8_t* ws, uint64_t limit_ns,
+// Launches compress_kernel over T tensors of WB-byte words into `out` (out_units words of
+// WB bytes). Every stream starts on a 4-byte boundary, so that the kernel can write headers
+// and tables as 32-bit words: with WB = 4 every position is one, and WB = 2 is a single
+// stream at `out` (4-byte aligned; checked by the caller).
+template <int MAXT, int WB>
+zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, void* out,
+                    uint64_t out_units, uint64_t* out_size, uint8_t* ws, uint64_t limit_ns,
                     cudaStream_t stream) {
-  CompressArgs<MAXT> args;
-  args.out = out;
-  args.out_words = out_words;
+  using Word = typename CompressArgs<MAXT, WB>::Word;
+  static_assert(WB == 4 || MAXT == 1, "16-bit words: single streams only");
+  CompressArgs<MAXT, WB> args;
+  args.out = static_cast<Word*>(out);
+  args.out_words = out_units;
   args.out_size = out_size;
   args.ws = ws;
   args.wait_limit_ns = limit_ns;
@@ -615,14 +716,15 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
   args.batched = batched ? 1u : 0u;
   args.inner_chunks = C % kTileElems != 0 ? 1u : 0u;
   uint64_t tiles = 0;
-  uint64_t hdr = batched ? (kBatchHeaderWords + 2 * ((uint64_t)T + 1)) : 0;
+  // header, tables and batch prefix in units of WB bytes
+  uint64_t hdr = batched ? (4 * kBatchHeaderWords + 8 * ((uint64_t)T + 1)) / WB : 0;
   for (uint32_t i = 0; i < T; ++i) {
-    args.in[i] = ts[i].ptr;
+    args.in[i] = static_cast<const Word*>(ts[i].ptr);
     args.n[i] = ts[i].n;
     args.tile_begin[i] = tiles;
     args.hdr_before[i] = hdr;
     tiles += tiles_for(ts[i].n);
-    hdr += kStreamHeaderWords + 2 * ceil_div_u64(ts[i].n, C);
+    hdr += (4 * kStreamHeaderWords + 8 * ceil_div_u64(ts[i].n, C)) / WB;
     args.payload_base[i] = hdr;
   }
   args.tile_begin[T] = tiles;
@@ -632,20 +734,20 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
   // CTAs of this kernel that fit on the current device at once, found once per device
   constexpr int kMaxDevices = 64;
   static std::atomic<int> resident_of[kMaxDevices];
-  const int smem = (int)sizeof(CompressShared);
+  const int smem = (int)sizeof(CompressShared<WB>);
   cudaError_t e;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_failure(e);
   if (dev < 0 || dev >= kMaxDevices) return ZVC_ERR_INVALID_ARG;
   int resident = resident_of[dev].load();
   if (resident == 0) {
-    e = cudaFuncSetAttribute(compress_kernel<MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(compress_kernel<MAXT, WB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return cuda_failure(e);
     int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_failure(e);
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel<MAXT>,
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel<MAXT, WB>,
                                                            kRoleThreads, smem)) != cudaSuccess)
       return cuda_failure(e);
     resident = sms * (per_sm > 0 ? per_sm : 1);
@@ -663,7 +765,7 @@ zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, ui
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const TraceMark mark = trace_begin(kTraceCompress, stream);
-  e = cudaLaunchKernelEx(&cfg, compress_kernel<MAXT>, args);
+  e = cudaLaunchKernelEx(&cfg, compress_kernel<MAXT, WB>, args);
   trace_end(mark, stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_failure(e);
@@ -676,13 +778,21 @@ zvc_status launch_compress(const TensorIn* ts, uint32_t T, bool batched, uint32_
                            uint32_t* out, uint64_t out_words, uint64_t* out_size, uint8_t* ws,
                            uint64_t wait_limit_ns, cudaStream_t stream) {
   if (!batched && T == 1)
-    return launch_t<1>(ts, T, false, chunk_elems, out, out_words, out_size, ws, wait_limit_ns,
-                       stream);
+    return launch_t<1, 4>(ts, T, false, chunk_elems, out, out_words, out_size, ws, wait_limit_ns,
+                          stream);
   if (T <= 64)
-    return launch_t<64>(ts, T, batched, chunk_elems, out, out_words, out_size, ws, wait_limit_ns,
+    return launch_t<64, 4>(ts, T, batched, chunk_elems, out, out_words, out_size, ws,
+                           wait_limit_ns, stream);
+  return launch_t<ZVC_MAX_BATCH, 4>(ts, T, batched, chunk_elems, out, out_words, out_size, ws,
+                                    wait_limit_ns, stream);
+}
+
+zvc_status launch_compress16(const uint16_t* in, uint64_t n, uint32_t chunk_elems, uint16_t* out,
+                             uint64_t out_units, uint64_t* out_size, uint8_t* ws,
+                             uint64_t wait_limit_ns, cudaStream_t stream) {
+  const TensorIn t{in, n};
+  return launch_t<1, 2>(&t, 1, false, chunk_elems, out, out_units, out_size, ws, wait_limit_ns,
                         stream);
-  return launch_t<ZVC_MAX_BATCH>(ts, T, batched, chunk_elems, out, out_words, out_size, ws,
-                                 wait_limit_ns, stream);
 }
 
 zvc_status launch_lookback_timeout_probe(uint8_t* ws, uint64_t limit_ns, cudaStream_t stream) {

@@ -61,7 +61,14 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
   return done != 0;
 }
 
-template <int MAXT>
+// WB is the word size in bytes: 4 (any 32-bit type) or 2 (bf16 / fp16, single streams).
+// Positions inside a chunk are counted in units of one word; a mask is 4 / WB units, and a
+// 16-byte group holds 16 / WB units.
+template <int WB> struct WordOf;
+template <> struct WordOf<4> { using T = uint32_t; };
+template <> struct WordOf<2> { using T = uint16_t; };
+
+template <int MAXT, int WB>
 struct DecompressArgs {
   const uint32_t* in;
   uint64_t in_bytes;
@@ -76,7 +83,7 @@ struct DecompressArgs {
   uint32_t meta_offset_words;  // window table, 8-byte aligned
   uint32_t chunks_per_cta;
   uint32_t slot_words;         // shared memory of one chunk: control, buffer, table
-  uint32_t* out[MAXT];
+  typename WordOf<WB>::T* out[MAXT];
   uint64_t n[MAXT];
   uint64_t chunk_begin[MAXT + 1];
 };
@@ -97,11 +104,14 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
 
 // One thread per chunk: validate, stage and walk. Returns with ctl.state set to 1 (table
 // complete and checked) or 2 (give up; an error is latched unless the item had no chunk).
-template <int MAXT>
-__device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32_t* dsm,
+template <int MAXT, int WB>
+__device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, uint32_t* dsm,
                        Control* ec, uint64_t item) {
+  using Word = typename WordOf<WB>::T;
+  constexpr uint32_t MU = 4u / WB;   // units of a mask
+  constexpr uint32_t UPG = 16u / WB; // units of a 16-byte group
   const uint32_t C = a.chunk_elems;
-  uint32_t* buf = dsm + kCtlWords;
+  Word* buf = reinterpret_cast<Word*>(dsm + kCtlWords);
   uint2* wmeta = reinterpret_cast<uint2*>(dsm + kCtlWords + a.meta_offset_words);
   const bool is_chunk = item < a.total_chunks;
   uint32_t ti = 0;
@@ -174,46 +184,47 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
     start = get_u64_words(ct);
     if (c + 1 < nc) end = get_u64_words(ct + 2);
   }
-  ok = (h[0] == kStreamMagic) & (h[1] == kVersionWordBytes) & (h[2] == kWindow) & (h[3] == C) &
+  ok = (h[0] == kStreamMagic) & (h[1] == (1u | ((uint32_t)WB << 16))) & (h[2] == kWindow) &
+       (h[3] == C) &
        (((uint64_t)h[4] | ((uint64_t)h[5] << 32)) == n) &
        (((uint64_t)h[6] | ((uint64_t)h[7] << 32)) == payload);
   if (is_chunk)
     ok = ok & ((c != 0) | (start == 0)) & (start <= end) & (end <= payload) &
-         (((start | end) & 3u) == 0) && (end - start) / 4 >= nwin &&
-         (end - start) / 4 <= (uint64_t)nwin + count;
+         (((start | end) & (uint64_t)(WB - 1)) == 0) && (end - start) / WB >= (uint64_t)MU * nwin &&
+         (end - start) / WB <= (uint64_t)MU * nwin + count;
   if (!ok || !is_chunk) {
     give_up(ok ? 0u : (uint32_t)ZVC_ERR_CORRUPT);
     return;
   }
 
-  // ---- stage the chunk: its words sit in shared memory at the same 16-byte phase as in
+  // ---- stage the chunk: its units sit in shared memory at the same 16-byte phase as in
   // global memory, so one bulk copy moves the aligned body and plain loads the at most
-  // three words on either side. The buffer holds cap words; a longer chunk is staged in pieces
-  // (below), the first piece being its first cap - phase words.
-  const uint32_t len = (uint32_t)((end - start) / 4);
-  const uint32_t* cw = sw + kStreamHeaderWords + 2 * nc + start / 4;
-  const uint32_t cap = a.cap_words;
-  uint32_t ph = (uint32_t)((reinterpret_cast<uintptr_t>(cw) >> 2) & 3u);
-  uint32_t e = min(len, cap - ph);  // chunk words [s, e) are staged, s = 0 here
+  // UPG - 1 units on either side. The buffer holds cap units; a longer chunk is staged in
+  // pieces (below), the first piece being its first cap - phase units.
+  const uint32_t len = (uint32_t)((end - start) / WB);
+  const Word* cw = reinterpret_cast<const Word*>(sw) + (4ull * kStreamHeaderWords + 8 * nc + start) / WB;
+  const uint32_t cap = a.cap_words * (4u / WB);
+  uint32_t ph = (uint32_t)((reinterpret_cast<uintptr_t>(cw) / WB) & (UPG - 1));
+  uint32_t e = min(len, cap - ph);  // chunk units [s, e) are staged, s = 0 here
   uint32_t fills = 0;                // bulk copies completed on ctl.full (its phase)
   {
-    const uint32_t head = min(e, (4u - ph) & 3u);
-    const uint32_t body = (e - head) & ~3u;
+    const uint32_t head = min(e, (UPG - ph) & (UPG - 1));
+    const uint32_t body = (e - head) & ~(UPG - 1);
     const uint32_t tail = e - head - body;
-    uint32_t x[6];
+    Word x[2 * (UPG - 1)];
 #pragma unroll
-    for (uint32_t i = 0; i < 3; ++i) {
-      x[i] = i < head ? __ldcs(cw + i) : 0u;
-      x[3 + i] = i < tail ? __ldcs(cw + head + body + i) : 0u;
+    for (uint32_t i = 0; i < UPG - 1; ++i) {
+      x[i] = i < head ? __ldcs(cw + i) : (Word)0;
+      x[UPG - 1 + i] = i < tail ? __ldcs(cw + head + body + i) : (Word)0;
     }
     if (body > 0) {
-      mbar_arrive_expect_tx(&ctl.full, body * 4);
-      bulk_g2s(buf + ph + head, cw + head, body * 4, &ctl.full);
+      mbar_arrive_expect_tx(&ctl.full, body * WB);
+      bulk_g2s(buf + ph + head, cw + head, body * WB, &ctl.full);
     }
 #pragma unroll
-    for (uint32_t i = 0; i < 3; ++i) {
+    for (uint32_t i = 0; i < UPG - 1; ++i) {
       if (i < head) buf[ph + i] = x[i];
-      if (i < tail) buf[ph + head + body + i] = x[3 + i];
+      if (i < tail) buf[ph + head + body + i] = x[UPG - 1 + i];
     }
     if (body > 0 && !mbar_wait(&ctl.full, 0, a.wait_limit_ns)) {
       give_up(ZVC_ERR_TIMEOUT);
@@ -240,23 +251,28 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
   unsigned long long* wm = reinterpret_cast<unsigned long long*>(wmeta);
   uint32_t s = 0, bp = ph, m = 0, w = 0, piece = 1;
   bool good = true;
+  // the mask at unit p (for WB = 2 it may sit on a 2-byte boundary: two 16-bit loads)
+  auto mask_at = [&](uint32_t p) -> uint32_t {
+    if (WB == 4) return (uint32_t)buf[p];
+    return (uint32_t)buf[p] | ((uint32_t)buf[p + 1] << 16);
+  };
   while (w < nwin) {
-    const uint32_t k = min(nwin - w, (cap - bp) / (kWindow + 1));
+    const uint32_t k = min(nwin - w, (cap - bp) / (kWindow + MU));
     if (k > 0) {
       const uint32_t w1 = w + k;
 #pragma unroll 4
       for (; w < w1; ++w) {
-        m = buf[bp];
-        wm[w] = (unsigned long long)(bp + 1u) | ((unsigned long long)m << 32);
-        bp += 1u + __popc(m);
+        m = mask_at(bp);
+        wm[w] = (unsigned long long)(bp + MU) | ((unsigned long long)m << 32);
+        bp += MU + __popc(m);
       }
       continue;
     }
-    if (bp < cap) {
-      m = buf[bp];
-      const uint32_t nb = bp + 1u + __popc(m);
+    if (bp + MU <= cap) {
+      m = mask_at(bp);
+      const uint32_t nb = bp + MU + __popc(m);
       if (nb <= cap) {
-        wm[w] = (unsigned long long)(bp + 1u) | ((unsigned long long)m << 32);
+        wm[w] = (unsigned long long)(bp + MU) | ((unsigned long long)m << 32);
         bp = nb;
         ++w;
         continue;
@@ -280,26 +296,26 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
       __nanosleep(64);
     }
     fence_proxy_async_smem();  // the scatterer's reads come before the copy's writes
-    // The piece starts at this window's 16-byte group: the at most three words before it
+    // The piece starts at this window's 16-byte group: the at most UPG - 1 units before it
     // are the stream's (a chunk is preceded by the header and table at least), so one bulk
     // copy moves every whole group that fits; a piece that reaches the chunk's end loads
-    // the words past its last group with plain loads, under the copy.
+    // the units past its last group with plain loads, under the copy.
     s = pos;
-    ph = (uint32_t)((reinterpret_cast<uintptr_t>(cw + s) >> 2) & 3u);
-    const uint32_t* src = cw + s - ph;                // 16-byte aligned
-    const uint32_t n = min(len - s + ph, cap);        // words of this piece, from src
-    const uint32_t body = n & ~3u;                    // cap is a multiple of 4
-    const uint32_t rest = n - body;                   // only at the chunk's end: <= 3
+    ph = (uint32_t)((reinterpret_cast<uintptr_t>(cw + s) / WB) & (UPG - 1));
+    const Word* src = cw + s - ph;                    // 16-byte aligned
+    const uint32_t n = min(len - s + ph, cap);        // units of this piece, from src
+    const uint32_t body = n & ~(UPG - 1);             // cap is a multiple of UPG
+    const uint32_t rest = n - body;                   // only at the chunk's end: < UPG
     e = s - ph + n;
-    uint32_t x[3];
+    Word x[UPG - 1];
 #pragma unroll
-    for (uint32_t i = 0; i < 3; ++i) x[i] = i < rest ? __ldcs(src + body + i) : 0u;
+    for (uint32_t i = 0; i < UPG - 1; ++i) x[i] = i < rest ? __ldcs(src + body + i) : (Word)0;
     if (body > 0) {
-      mbar_arrive_expect_tx(&ctl.full, body * 4);
-      bulk_g2s(buf, src, body * 4, &ctl.full);
+      mbar_arrive_expect_tx(&ctl.full, body * WB);
+      bulk_g2s(buf, src, body * WB, &ctl.full);
     }
 #pragma unroll
-    for (uint32_t i = 0; i < 3; ++i)
+    for (uint32_t i = 0; i < UPG - 1; ++i)
       if (i < rest) buf[body + i] = x[i];
     if (body > 0) {
       if (!mbar_wait(&ctl.full, fills & 1u, a.wait_limit_ns)) {
@@ -320,8 +336,8 @@ __device__ void walker(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32
 }
 
 // Warp 1: expands the recorded windows of its chunk as the walker records them.
-template <int MAXT>
-__device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uint32_t* dsm,
+template <int MAXT, int WB>
+__device__ void scatterer(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, uint32_t* dsm,
                           Control* ec, uint64_t item, uint32_t lane) {
   if (item >= a.total_chunks) return;  // header checks only: the walker does them
   const uint32_t C = a.chunk_elems;
@@ -337,12 +353,17 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
   const uint64_t c = item - a.chunk_begin[ti];
   const uint64_t cbeg = c * C;
   const uint32_t count = (uint32_t)min((uint64_t)C, a.n[ti] - cbeg);
+  using Word = typename WordOf<WB>::T;
+  constexpr uint32_t EPL = 16u / WB;       // units a lane expands: one 16-byte store
+  constexpr uint32_t LPW = kWindow / EPL;  // lanes per window: 8 (WB = 4) or 4 (WB = 2)
+  constexpr uint32_t WPI = 32u / LPW;      // windows per pass of the warp: 4 or 8
+  constexpr int KW = (int)(kPublishEvery / WPI);  // passes per group of 16 windows
   const uint32_t nwin = (count + kWindow - 1) / kWindow;
-  const uint32_t* buf = dsm + kCtlWords;
+  const Word* buf = reinterpret_cast<const Word*>(dsm + kCtlWords);
   const uint2* wmeta = reinterpret_cast<const uint2*>(dsm + kCtlWords + a.meta_offset_words);
-  uint32_t* dst = a.out[ti] + cbeg;
+  Word* dst = a.out[ti] + cbeg;
   const bool vec = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
-  const uint32_t e = 4u * (lane & 7u);
+  const uint32_t e = EPL * (lane % LPW);
   const uint32_t below = (1u << e) - 1u;
   uint64_t t0 = 0;
   // bounded wait for the walker; false: give up (the walker gave up, or the wait ran out)
@@ -376,51 +397,60 @@ __device__ void scatterer(const DecompressArgs<MAXT>& a, DecompressCtl& ctl, uin
   uint32_t g0 = 0, handled = 0;
   while (g0 < nwin) {
     const uint32_t need = min(nwin, g0 + kPublishEvery);
-    // the group's windows: lane group l/8 takes windows g0 + l/8 + 4k, k = 0..3; each lane
+    // the group's windows: lane group l/LPW takes windows g0 + l/LPW + WPI k; each lane
     // waits (bounded) until the walker has recorded its windows, or until the walker asks
     // for the windows before d to be expanded (it stages the next piece from window d)
-    unsigned long long ent[4];
+    unsigned long long ent[KW];
     uint32_t lim, d;
     while (true) {
       d = *drain;
       lim = (d > handled && d <= need) ? d : need;
       bool all = true;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t w = g0 + (lane >> 3) + 4u * k;
+      for (int k = 0; k < KW; ++k) {
+        const uint32_t w = g0 + lane / LPW + WPI * k;
         ent[k] = w < lim ? wm[w] : 1ull;
         all &= (uint32_t)ent[k] != 0u;
       }
       if (__all_sync(0xffffffffu, all)) break;
       if (!waited(kPollSleepNs)) return;
     }
-    uint4 r[4];
+    uint4 r[KW];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t w = g0 + (lane >> 3) + 4u * k;
+    for (int k = 0; k < KW; ++k) {
+      const uint32_t w = g0 + lane / LPW + WPI * k;
       const uint32_t m = w < lim ? (uint32_t)(ent[k] >> 32) : 0u;
       uint32_t q = (uint32_t)ent[k] + __popc(m & below);
-      uint32_t v[4];
+      uint32_t v[EPL];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (uint32_t j = 0; j < EPL; ++j) {
         const uint32_t bit = (m >> (e + j)) & 1u;
-        v[j] = bit ? buf[q] : 0u;
+        v[j] = bit ? (uint32_t)buf[q] : 0u;
         q += bit;
       }
-      r[k] = make_uint4(v[0], v[1], v[2], v[3]);
+      if constexpr (WB == 4)
+        r[k] = make_uint4(v[0], v[1], v[2], v[3]);
+      else
+        r[k] = make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16),
+                          v[6] | (v[7] << 16));
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t w = g0 + (lane >> 3) + 4u * k;
+    for (int k = 0; k < KW; ++k) {
+      const uint32_t w = g0 + lane / LPW + WPI * k;
       if (w >= lim) break;
       const uint32_t base = w * kWindow + e;
-      if (vec && base + 4u <= count) {
+      if (vec && base + EPL <= count) {
         *reinterpret_cast<uint4*>(dst + base) = r[k];
       } else {
         const uint32_t vv[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
 #pragma unroll
-        for (uint32_t j = 0; j < 4; ++j)
-          if (base + j < count) dst[base + j] = vv[j];
+        for (uint32_t j = 0; j < EPL; ++j) {
+          if constexpr (WB == 4) {
+            if (base + j < count) dst[base + j] = vv[j];
+          } else {
+            if (base + j < count) dst[base + j] = (Word)(vv[j / 2] >> (16u * (j & 1u)));
+          }
+        }
       }
     }
     g0 = lim;
@@ -445,9 +475,9 @@ constexpr uint32_t kMaxThreads = 32 * (1 + plan::kMaxChunksPerCta);
 constexpr uint32_t kSmallChunkElems = 1024;
 constexpr uint32_t kSmallMinCtas = 10;
 
-template <int MAXT, bool SMALL>
+template <int MAXT, int WB, bool SMALL>
 __global__ void __launch_bounds__(kMaxThreads, SMALL ? kSmallMinCtas : 0)
-    decompress_kernel(const __grid_constant__ DecompressArgs<MAXT> a) {
+    decompress_kernel(const __grid_constant__ DecompressArgs<MAXT, WB> a) {
   extern __shared__ __align__(16) uint32_t dsm_all[];
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   // this thread's chunk within the CTA: lane k of warp 0 walks chunk k, warp k + 1
@@ -511,10 +541,11 @@ zvc_status device_limits(plan::Limits* d) {
   return ZVC_OK;
 }
 
-template <int MAXT, bool SMALL>
+template <int MAXT, int WB, bool SMALL>
 zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, uint32_t T,
                     bool batched, uint32_t C, uint8_t* ws, cudaStream_t stream) {
-  DecompressArgs<MAXT> args;
+  static_assert(WB == 4 || MAXT == 1, "16-bit words: single streams only");
+  DecompressArgs<MAXT, WB> args;
   args.in = in;
   args.in_bytes = in_bytes;
   args.ws = ws;
@@ -524,7 +555,7 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   args.batched = batched ? 1u : 0u;
   uint64_t chunks = 0;
   for (uint32_t i = 0; i < T; ++i) {
-    args.out[i] = ts[i].ptr;
+    args.out[i] = static_cast<typename WordOf<WB>::T*>(ts[i].ptr);
     args.n[i] = ts[i].n;
     args.chunk_begin[i] = chunks;
     chunks += ceil_div_u64(ts[i].n, C);
@@ -533,7 +564,7 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   args.total_chunks = chunks;
   args.total_items = chunks + (batched && T == 0 ? 1 : T);
   const uint32_t wpc = C / kWindow;
-  const uint32_t full_cap = plan::full_cap_words(C);
+  const uint32_t full_cap = plan::full_cap_words(C, WB);
   plan::Limits d;
   zvc_status st = device_limits(&d);
   if (st != ZVC_OK) return st;
@@ -541,10 +572,10 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   // limit), and all of the SM's unified memory as shared memory
   const uint64_t most = plan::slot_bytes(full_cap, C) * plan::kMaxChunksPerCta;
   cudaError_t e = cudaFuncSetAttribute(
-      decompress_kernel<MAXT, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      decompress_kernel<MAXT, WB, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)min(most, (uint64_t)d.smem_per_cta_max));
   if (e != cudaSuccess) return cuda_failure(e);
-  e = cudaFuncSetAttribute(decompress_kernel<MAXT, SMALL>,
+  e = cudaFuncSetAttribute(decompress_kernel<MAXT, WB, SMALL>,
                            cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return cuda_failure(e);
   // the buffer's size and the chunks per CTA, with the occupancy the runtime reports
@@ -552,7 +583,7 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   auto occ = [&](uint32_t k, uint32_t cap) -> int {
     int n = 0;
     const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &n, decompress_kernel<MAXT, SMALL>, (int)(32 * (1 + k)),
+        &n, decompress_kernel<MAXT, WB, SMALL>, (int)(32 * (1 + k)),
         (size_t)(k * plan::slot_bytes(cap, C)));
     if (r != cudaSuccess) {
       occ_err = r;
@@ -561,7 +592,7 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
     return n;
   };
   plan::Plan pl;
-  if (!plan::decompress_plan(chunks, in_bytes, T, batched, C, d, occ, &pl))
+  if (!plan::decompress_plan(chunks, in_bytes, T, batched, C, d, occ, &pl, WB))
     return cuda_failure(occ_err);
   args.cap_words = pl.cap_words;
   args.chunks_per_cta = pl.chunks_per_cta;
@@ -571,19 +602,19 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   const uint32_t threads = 32u * (1u + args.chunks_per_cta);
   const uint64_t blocks = ceil_div_u64(args.total_items, args.chunks_per_cta);
   const TraceMark mark = trace_begin(kTraceDecompress, stream);
-  decompress_kernel<MAXT, SMALL><<<(unsigned)blocks, threads, smem, stream>>>(args);
+  decompress_kernel<MAXT, WB, SMALL><<<(unsigned)blocks, threads, smem, stream>>>(args);
   trace_end(mark, stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_failure(e);
   return ZVC_OK;
 }
 
-template <int MAXT>
+template <int MAXT, int WB>
 zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, uint32_t T,
                     bool batched, uint32_t C, uint8_t* ws, cudaStream_t stream) {
   if (C <= kSmallChunkElems)
-    return launch_k<MAXT, true>(in, in_bytes, ts, T, batched, C, ws, stream);
-  return launch_k<MAXT, false>(in, in_bytes, ts, T, batched, C, ws, stream);
+    return launch_k<MAXT, WB, true>(in, in_bytes, ts, T, batched, C, ws, stream);
+  return launch_k<MAXT, WB, false>(in, in_bytes, ts, T, batched, C, ws, stream);
 }
 
 }  // namespace
@@ -591,9 +622,16 @@ zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
 zvc_status launch_decompress(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts,
                              uint32_t T, bool batched, uint32_t chunk_elems, uint8_t* ws,
                              cudaStream_t stream) {
-  if (!batched && T == 1) return launch_t<1>(in, in_bytes, ts, T, false, chunk_elems, ws, stream);
-  if (T <= 64) return launch_t<64>(in, in_bytes, ts, T, batched, chunk_elems, ws, stream);
-  return launch_t<ZVC_MAX_BATCH>(in, in_bytes, ts, T, batched, chunk_elems, ws, stream);
+  if (!batched && T == 1)
+    return launch_t<1, 4>(in, in_bytes, ts, T, false, chunk_elems, ws, stream);
+  if (T <= 64) return launch_t<64, 4>(in, in_bytes, ts, T, batched, chunk_elems, ws, stream);
+  return launch_t<ZVC_MAX_BATCH, 4>(in, in_bytes, ts, T, batched, chunk_elems, ws, stream);
+}
+
+zvc_status launch_decompress16(const uint32_t* in, uint64_t in_bytes, uint16_t* out, uint64_t n,
+                               uint32_t chunk_elems, uint8_t* ws, cudaStream_t stream) {
+  const TensorOut t{out, n};
+  return launch_t<1, 2>(in, in_bytes, &t, 1, false, chunk_elems, ws, stream);
 }
 
 }  // namespace zvc

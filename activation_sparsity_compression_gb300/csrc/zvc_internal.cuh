@@ -34,8 +34,8 @@ struct Control {
 constexpr uint64_t kControlBytes = 256;
 constexpr uint64_t kStatusOffset = 512;
 
-// Tile status word: the launch's epoch in bits 63..16 and the tile's payload words (an
-// aggregate: at most 4224) in bits 15..0.
+// Tile status word: the launch's epoch in bits 63..16 and the tile's payload units (an
+// aggregate: at most 4224 four-byte or 4352 two-byte units) in bits 15..0.
 constexpr uint32_t kAggBits = 16;
 constexpr uint64_t kAggMask = (1ull << kAggBits) - 1;
 constexpr uint64_t kEpochLimit = 1ull << (64 - kAggBits);
@@ -264,11 +264,11 @@ void trace_end(TraceMark m, cudaStream_t stream);
 
 // ------------------------------------------------------------------ launch plans
 struct TensorIn {
-  const uint32_t* ptr;
+  const void* ptr;  // n words of 4 (or, for the 16-bit calls, 2) bytes
   uint64_t n;
 };
 struct TensorOut {
-  uint32_t* ptr;
+  void* ptr;  // n words of 4 (or, for the 16-bit calls, 2) bytes
   uint64_t n;
 };
 
@@ -277,10 +277,19 @@ zvc_status launch_compress(const TensorIn* ts, uint32_t T, bool batched, uint32_
                            uint32_t* out, uint64_t out_words, uint64_t* out_size, uint8_t* ws,
                            uint64_t wait_limit_ns, cudaStream_t stream);
 
+// Compress n 16-bit words into one stream at `out` (4-byte aligned; out_units 2-byte units).
+zvc_status launch_compress16(const uint16_t* in, uint64_t n, uint32_t chunk_elems, uint16_t* out,
+                             uint64_t out_units, uint64_t* out_size, uint8_t* ws,
+                             uint64_t wait_limit_ns, cudaStream_t stream);
+
 // Decompress a single stream (!batched, T == 1) or a batch of T streams.
 zvc_status launch_decompress(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts,
                              uint32_t T, bool batched, uint32_t chunk_elems, uint8_t* ws,
                              cudaStream_t stream);
+
+// Decompress one stream of 16-bit words (the stream at `in` is 4-byte aligned).
+zvc_status launch_decompress16(const uint32_t* in, uint64_t in_bytes, uint16_t* out, uint64_t n,
+                               uint32_t chunk_elems, uint8_t* ws, cudaStream_t stream);
 
 // RLE comparison codec (window of W words, 32 <= W <= ZVC_RLE_MAX_WINDOW).
 uint64_t rle_ws_bytes(uint64_t n, uint32_t W);

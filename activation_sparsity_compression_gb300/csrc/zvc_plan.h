@@ -34,8 +34,10 @@ struct Plan {
 
 inline uint64_t round_up4(uint64_t x) { return (x + 3) & ~3ull; }
 
-// The largest valid chunk of C elements (C/32 masks + C words) at any 16-byte phase.
-inline uint32_t full_cap_words(uint32_t C) {
+// The largest valid chunk of C elements (C/32 masks + C words of wb bytes) in 4-byte words,
+// at any 16-byte phase (and, for 2-byte words, starting on either half of a 4-byte word).
+inline uint32_t full_cap_words(uint32_t C, uint32_t wb = 4) {
+  if (wb == 2) return (uint32_t)round_up4((uint64_t)C / kWindowWords + C / 2 + 4);
   return (uint32_t)round_up4((uint64_t)C / kWindowWords + C + 3);
 }
 
@@ -69,8 +71,8 @@ inline uint64_t mean_chunk_words(uint64_t in_bytes, uint64_t chunks, uint32_t T,
 //   stages fewer chunks in pieces.
 template <class Occ>
 bool decompress_plan(uint64_t chunks, uint64_t in_bytes, uint32_t T, bool batched, uint32_t C,
-                     const Limits& d, Occ occ, Plan* out) {
-  const uint32_t full_cap = full_cap_words(C);
+                     const Limits& d, Occ occ, Plan* out, uint32_t wb = 4) {
+  const uint32_t full_cap = full_cap_words(C, wb);
   out->cap_words = full_cap;
   out->chunks_per_cta = 1;
   if (chunks == 0) return true;

@@ -156,6 +156,34 @@ zvc_status zvc_decompress_batched(const void* d_in, uint64_t in_bytes, void* con
                                   const uint64_t* ns, uint32_t T, uint32_t chunk_elems,
                                   void* d_ws, uint64_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------------
+ * ZVC on 16-bit words (bf16 / fp16). Section V.A "Compression Algorithm" gives the rule
+ * for the 32-bit activations the paper evaluates; these calls apply it unchanged to 2-byte
+ * words, a reading beyond the pages: 32 values per window, one 32-bit mask, then the
+ * non-zero 2-byte values in ascending element order. The stream is the format above with
+ * word_bytes = 2: windows follow each other without padding, so a mask may start on a
+ * 2-byte boundary, and chunk offsets are even byte counts. A word is zero iff its 16 bits
+ * are clear (-0.0 = 0x8000 is kept). Size: 32 + 8*ceil(n/C) + 4*ceil(n/32) + 2*nnz.
+ * Single streams only (no batch, no offload). The workspace is zvc_workspace_size(n, C). */
+
+/* Worst case of one 16-bit stream (every word non-zero), as in section V.A: 32 + 8*ceil(n/C)
+ * + 4*ceil(n/32) + 2*n. Returns 0 if chunk_elems is invalid. */
+uint64_t zvc_size_bound16(uint64_t n, uint32_t chunk_elems);
+
+/* Compress n 16-bit words at d_in (2-byte aligned) into one stream at d_out (4-byte aligned;
+ * out_cap >= zvc_size_bound16(n, C)); the byte count goes to the device u64 *d_out_size
+ * (may be NULL). Section V.A on 2-byte words, as above. Errors as for zvc_compress. */
+zvc_status zvc_compress16(const void* d_in, uint64_t n, uint32_t chunk_elems, void* d_out,
+                          uint64_t out_cap, uint64_t* d_out_size, void* d_ws, uint64_t ws_bytes,
+                          void* stream);
+
+/* Decompress a 16-bit stream of in_bytes bytes at d_in (4-byte aligned) into n words at
+ * d_out (2-byte aligned): the inverse of section V.A on 2-byte words. A stream that is not
+ * a valid 16-bit encoding of n words with chunk_elems C latches ZVC_ERR_CORRUPT, with no
+ * access outside [d_in, d_in + in_bytes) or [d_out, d_out + 2n). */
+zvc_status zvc_decompress16(const void* d_in, uint64_t in_bytes, void* d_out, uint64_t n,
+                            uint32_t chunk_elems, void* d_ws, uint64_t ws_bytes, void* stream);
+
 /* Segment length (words) that zvc_offload uses for a tensor of n words: n cut into
  * ceil(n / 2^25) equal parts, rounded up to whole chunks (at most about 32 Mi words,
  * 128 MiB of fp32). Cites section V.D "Software Interface": compression throughput must

@@ -115,5 +115,5 @@ def test_every_declaration_cites_its_passage():
         # the last comment block that opens a line above the declaration (a trailing
         # comment on a #define line is not one)
         blocks = [c for c in re.finditer(r"^/\*.*?\*/", text, re.M | re.S) if c.end() <= m.start()]
-        comment = blocks[-1].group(0)
+        comment = blocks[-1].group(0).lower()
         assert ("section" in comment) or ("no counterpart" in comment), name
