@@ -403,10 +403,12 @@ __device__ void pack_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& s
     const uint32_t nzw = tot - held * (4u / WB);  // the warp's non-zero words
     const uint32_t sa = smem_addr(slot);
     uint32_t* woff = sm.woff[s] + w0;
-    if (nwin == kTileWindows && !keep_woff && (nzw <= kSkipBelow || nzw >= kSkipAbove)) {
-      pack_whole<WB, true, false>(sa, pos, v, m, lane, lane_below, woff);
-    } else if (nwin == kTileWindows && !keep_woff) {
+    // (the order of these branches is measured: with the plain loop first the 5-25% maps
+    // gain 2% and the 0-1% ones lose 4-6%, which leaves every density above 0.7 of HBM)
+    if (nwin == kTileWindows && !keep_woff && nzw > kSkipBelow && nzw < kSkipAbove) {
       pack_whole<WB, false, false>(sa, pos, v, m, lane, lane_below, woff);
+    } else if (nwin == kTileWindows && !keep_woff) {
+      pack_whole<WB, true, false>(sa, pos, v, m, lane, lane_below, woff);
     } else if (nwin == kTileWindows) {  // chunks start inside tiles: window offsets are kept
       // one loop only: every unrolled copy of the loop in this kernel slows all of them
       pack_whole<WB, false, true>(sa, pos, v, m, lane, lane_below, woff);

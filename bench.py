@@ -87,6 +87,10 @@ def parse_args(argv=None):
                         "layers, VGG conv1_2, the 2^28-word density sweep, the 57-tensor "
                         "GoogLeNet batch in one batched launch each way); prints one JSON "
                         "line and exits")
+    p.add_argument("--configs16", action="store_true",
+                   help="the 16-bit calls (zvc_compress16 / zvc_decompress16) on bf16 copies of "
+                        "the single-tensor configurations (AlexNet layers, VGG conv1_2, the "
+                        "2^28-word density sweep); prints one JSON line and exits")
     p.add_argument("--write-traffic", nargs=2, metavar=("COMPRESS_CSV", "DECOMPRESS_CSV"),
                    help="turn ncu DRAM counters of one step's launches (see TRAFFIC_FILE) "
                         "into that file, keyed by the kernels' source hashes, and exit")
@@ -1146,6 +1150,82 @@ def run_configs(args):
     return 0
 
 
+def run_configs16(args):
+    """The 16-bit calls alone (device buffers, back-to-back launches) on bf16 copies of the
+    single-tensor configurations: each AlexNet layer, VGG conv1_2 at batch 64, and the
+    2^28-word density sweep (i.i.d. and 1024-word blocks). Algorithmic bytes are 2n + S.
+    Every case is checked bit-exact after decompression."""
+    import torch
+
+    from activation_sparsity_compression_gb300 import build as zbuild
+    zbuild.build()
+    import activation_sparsity_compression_gb300 as zvc
+    import workloads
+
+    C = args.chunk_elems
+    peak, peak_kind = hbm_peak()
+    sh = torch.cuda.current_stream().cuda_stream
+    cases = []
+
+    def single(name, x32, extra=None):
+        x = x32.to(torch.bfloat16).contiguous().view(-1)
+        del x32
+        n = x.numel()
+        cap = zvc.zvc_size_bound16(n, C)
+        out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+        size = torch.zeros(1, dtype=torch.int64, device="cuda")
+        ws = zvc.new_workspace(zvc.zvc_workspace_size(n, C))
+        y = torch.empty_like(x)
+
+        def comp():
+            zvc.zvc_compress16(x.data_ptr(), n, C, out.data_ptr(), cap, size.data_ptr(),
+                               ws.data_ptr(), ws.numel(), sh)
+        comp()
+        torch.cuda.synchronize()
+        S = int(size.item())
+
+        def decomp():
+            zvc.zvc_decompress16(out.data_ptr(), S, y.data_ptr(), n, C, ws.data_ptr(),
+                                 ws.numel(), sh)
+        tc, _ = _per_launch_ms(torch, comp)
+        td, _ = _per_launch_ms(torch, decomp)
+        if zvc.zvc_get_error(ws.data_ptr(), sh) != zvc.ZVC_OK or not torch.equal(
+                x.view(torch.int16), y.view(torch.int16)):
+            raise RuntimeError(f"{name}: 16-bit round trip is not bit-exact")
+        moved = 2 * n + S
+        c = {"case": name, "n_words": n, "stream_bytes": S, "ratio": 2 * n / S,
+             "compress_us": tc * 1e3, "decompress_us": td * 1e3,
+             "compress_gbs": 2 * n / (tc / 1e3) / 1e9, "decompress_gbs": 2 * n / (td / 1e3) / 1e9,
+             "compress_hbm_frac": moved / (tc / 1e3) / 1e9 / peak,
+             "decompress_hbm_frac": moved / (td / 1e3) / 1e9 / peak}
+        if extra:
+            c.update(extra)
+        cases.append(c)
+        print(json.dumps(c), file=sys.stderr, flush=True)
+        del out, y, ws, x
+
+    for l, x in enumerate(workloads.alexnet_stack(device="cuda")):
+        cc, hh, ww, d = workloads.ALEXNET_LAYERS[l]
+        single(f"alexnet layer {l} 128x{cc}x{hh}x{ww} ({int(d * 100)}% non-zero), bf16", x)
+    torch.cuda.empty_cache()
+    single("vgg_conv12 64x64x224x224, bf16", workloads.vgg_conv12(device="cuda")[0])
+    torch.cuda.empty_cache()
+    for structure in ("iid", "block"):
+        for d in workloads.SWEEP_DENSITIES:
+            x = workloads.density_sweep(d, structure, device="cuda")[0]
+            single(f"sweep 2^28 {structure} {d:.2f}, bf16", x, {"density": d, "structure": structure})
+            del x
+            torch.cuda.empty_cache()
+    print(json.dumps({"metric": "ZVC on 16-bit words, compress/decompress per configuration",
+                      "unit": "GB/s (uncompressed) and fraction of HBM", "peak": peak,
+                      "peak_kind": peak_kind, "chunk_elems": C, "word_bytes": 2,
+                      "data": "synthetic (bf16 copies of the fp32 configurations)",
+                      "timing": "CUDA events, one warm-up launch, best of 3 groups of 10 "
+                                "back-to-back launches",
+                      "cases": cases}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ training step with offload
 TRAIN_MODEL = ("deep CNN: conv 3->128 (3x3, stride 2) + ReLU, then 12 x (conv 128->128 3x3 + "
                "ReLU) at 112x112, global average pool, linear 128->1000; batch 64, 3x224x224, "
@@ -1336,6 +1416,8 @@ def main(argv=None):
         return write_traffic(args.write_traffic, args.chunk_elems, args.profile_batch)
     if args.configs:
         return run_configs(args)
+    if args.configs16:
+        return run_configs16(args)
     if args.train:
         return run_train(args)
     if args.layouts:
