@@ -116,6 +116,8 @@ struct __align__(16) CompressShared {
   uint64_t handoff[2];  // settle warps: tile i's inclusive prefix is in incl[i % 2]
   uint64_t incl[2];
   uint32_t incl_ok[2];
+  uint32_t incl_ti[2];   // ... and its tensor, and that tensor's start in the payload
+  uint64_t incl_pstart[2];
   uint64_t pbuf[ZVC_MAX_BATCH + 1];  // stream starts, for the headers
 };
 
@@ -452,12 +454,23 @@ __device__ void settle_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>&
     const uint32_t agg = f.agg, ti = f.ti;
     const uint64_t lt = f.lt;
     const int64_t floor = i ? (int64_t)(t - G) : -1;
-    uint64_t excl = 0;
-    bool ok = aggsum_finish<kLookbackWidth>(status, a.epoch, t, floor, lane, a.wait_limit_ns, ctl,
-                                            lb, &excl);
+    uint64_t excl = 0, since_start = 0;
+    // Batches: the payload units before the tile's stream (pstart). If the CTA's previous
+    // tile t - G lies in the same tensor, it is that tile's; otherwise the tensor's first
+    // tile lies inside this tile's look-back window (t - G, t), and pstart is excl less the
+    // aggregates from that first tile on, which the look-back reads anyway. So no tile
+    // waits for another CTA's settle.
+    bool ok = MAXT > 1 ? aggsum_finish<kLookbackWidth, true>(status, a.epoch, t, floor, lane,
+                                                             a.wait_limit_ns, ctl, lb, &excl,
+                                                             (int64_t)a.tile_begin[ti],
+                                                             &since_start)
+                       : aggsum_finish<kLookbackWidth>(status, a.epoch, t, floor, lane,
+                                                       a.wait_limit_ns, ctl, lb, &excl);
     if (t + 2 * G < a.total_tiles)  // start this warp's next pass
       aggsum_issue<kLookbackWidth>(status, a.epoch, (int64_t)(t + 2 * G) - 1, (int64_t)(t + G),
                                    lane, lb);
+    uint32_t prev_ti = ~0u;
+    uint64_t prev_pstart = 0;
     if (i > 0) {  // the CTA's previous tile, from the other settle warp
       const uint32_t h = (i - 1) & 1u;
       if (!mbar_wait(&sm.handoff[h], ((i - 1) / 2) & 1u, a.wait_limit_ns)) {
@@ -466,11 +479,17 @@ __device__ void settle_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>&
       }
       ok = ok && sm.incl_ok[h];
       excl += sm.incl[h];
+      prev_ti = sm.incl_ti[h];
+      prev_pstart = sm.incl_pstart[h];
     }
+    uint64_t pstart = 0;
+    if (MAXT > 1) pstart = lt == 0 ? excl : (prev_ti == ti ? prev_pstart : excl - since_start);
     __syncwarp();  // every lane has read the handoff before it is overwritten two tiles on
     if (lane == 0) {
       sm.incl[i & 1u] = excl + agg;
       sm.incl_ok[i & 1u] = ok;
+      sm.incl_ti[i & 1u] = ti;
+      sm.incl_pstart[i & 1u] = pstart;
       mbar_arrive(&sm.handoff[i & 1u]);
     }
     const uint64_t dst = a.payload_base[ti] + excl;
@@ -479,16 +498,9 @@ __device__ void settle_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>&
       ok = false;
     }
     if (lane == 0) {
-      uint64_t pstart = 0;
-      if (MAXT > 1) {
-        if (lt == 0) {
-          st_relaxed_u64(&tstart[ti].value, excl);
-          st_release_u64(&tstart[ti].tag, (a.epoch << 2) | (ok ? kStartPrefix : kStartError));
-          pstart = excl;
-        } else if (ok) {
-          // payload words before this tensor, published by its first tile (a lower tile)
-          ok = wait_tensor_start(a, tstart + ti, ctl, t, &pstart);
-        }
+      if (MAXT > 1 && lt == 0) {  // the headers need every stream's start (finalize_warp)
+        st_relaxed_u64(&tstart[ti].value, excl);
+        st_release_u64(&tstart[ti].tag, (a.epoch << 2) | (ok ? kStartPrefix : kStartError));
       }
       f.dst = dst;
       f.excl = excl;

@@ -141,23 +141,27 @@ __device__ __forceinline__ void aggsum_issue(const uint64_t* status, uint64_t ep
 }
 
 // Sum of the aggregates in (floor, tile) (warp-collective), starting from a pass `v`
-// already issued with top = tile - 1. Returns false (and latches ZVC_ERR_TIMEOUT) if an
+// already issued with top = tile - 1. With SUFFIX it also sums those of the tiles at or
+// above `from` into *suffix_out. Returns false (and latches ZVC_ERR_TIMEOUT) if an
 // aggregate is still missing after limit_ns.
-template <int K>
+template <int K, bool SUFFIX = false>
 __device__ __forceinline__ bool aggsum_finish(const uint64_t* status, uint64_t epoch, uint64_t tile,
                                               int64_t floor, uint32_t lane, uint64_t limit_ns,
-                                              Control* ctl, uint64_t (&v)[K], uint64_t* sum_out) {
-  uint64_t sum = 0;
+                                              Control* ctl, uint64_t (&v)[K], uint64_t* sum_out,
+                                              int64_t from = 0, uint64_t* suffix_out = nullptr) {
+  uint64_t sum = 0, suffix = 0;
   int64_t top = (int64_t)tile - 1;
   WaitClock clock;
   while (top > floor) {
     bool missing = false;
-    uint32_t part = 0;
+    uint32_t part = 0, spart = 0;
 #pragma unroll
     for (int j = 0; j < K; ++j) {
-      if (top - 32 * j - (int64_t)lane > floor) {
+      const int64_t idx = top - 32 * j - (int64_t)lane;
+      if (idx > floor) {
         missing |= (v[j] >> kAggBits) != epoch;
         part += (uint32_t)(v[j] & kAggMask);
+        if (SUFFIX && idx >= from) spart += (uint32_t)(v[j] & kAggMask);
       }
     }
     if (__any_sync(0xffffffffu, missing)) {
@@ -170,12 +174,14 @@ __device__ __forceinline__ bool aggsum_finish(const uint64_t* status, uint64_t e
       }
     } else {
       sum += __reduce_add_sync(0xffffffffu, part);
+      if (SUFFIX) suffix += __reduce_add_sync(0xffffffffu, spart);
       top -= 32 * K;
       if (top <= floor) break;
     }
     aggsum_issue<K>(status, epoch, top, floor, lane, v);
   }
   *sum_out = sum;
+  if (SUFFIX) *suffix_out = suffix;
   return true;
 }
 
