@@ -31,12 +31,21 @@
 namespace zvc {
 namespace {
 
-// Shared memory of a chunk's slot: control words, then the chunk buffer (cap words, at
-// most C/32 masks + C words + 3 for the 16-byte phase), then the window table (first
-// value, mask) per window. A CTA holds chunks_per_cta slots.
+// A work item is a group of up to `group` consecutive chunks of one tensor (group = 1 for
+// C >= 4096; for smaller chunks up to 8, so that an item covers up to 4096 elements): they
+// lie back to back in the stream, so one copy stages them and one walk decodes them, and
+// the per-item costs (locating and staging, a CTA's start) are paid once per group.
+//
+// Shared memory of an item's slot: control words, then the item's buffer (cap words, at
+// most its masks + words + 3 for the 16-byte phase), then the window table (first value,
+// mask) per window, then (grouped items only) kBndWords words where the walker keeps the
+// starts of the item's inner chunks. A CTA holds chunks_per_cta slots. Grouped items have
+// a kernel instantiation of their own (GRP), so the C >= 4096 kernel carries none of it.
+constexpr uint32_t kMaxGroup = 8;
+constexpr uint32_t kBndWords = kMaxGroup;
 struct DecompressCtl {
   uint64_t full;      // mbarrier of the TMA copies, one phase per bulk copy
-  uint32_t progress;  // pieces of the chunk staged so far
+  uint32_t progress;  // pieces of the item staged so far
   uint32_t state;     // 0 running, 1 walked and checked, 2 give up (nothing more to do)
   uint32_t drain;     // 0, or the window the next piece starts at (walker -> scatterer)
   uint32_t expanded;  // the windows before it are read out of the buffer (scatterer -> walker)
@@ -73,10 +82,11 @@ struct DecompressArgs {
   const uint32_t* in;
   uint64_t in_bytes;
   uint8_t* ws;
-  uint64_t total_chunks;
-  uint64_t total_items;  // total_chunks + T header checks
+  uint64_t total_chunks;  // work items that decode chunks (groups of up to `group` chunks)
+  uint64_t total_items;   // total_chunks + T header checks
   uint64_t wait_limit_ns;
   uint32_t chunk_elems;
+  uint32_t group;         // chunks per work item
   uint32_t T;
   uint32_t batched;
   uint32_t cap_words;          // chunk buffer words (a multiple of 4): longer chunks go in pieces
@@ -85,7 +95,7 @@ struct DecompressArgs {
   uint32_t slot_words;         // shared memory of one chunk: control, buffer, table
   typename WordOf<WB>::T* out[MAXT];
   uint64_t n[MAXT];
-  uint64_t chunk_begin[MAXT + 1];
+  uint64_t chunk_begin[MAXT + 1];  // first work item of tensor i
 };
 
 __device__ __forceinline__ uint64_t get_u64_words(const uint32_t* p) {
@@ -104,13 +114,14 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
 
 // One thread per chunk: validate, stage and walk. Returns with ctl.state set to 1 (table
 // complete and checked) or 2 (give up; an error is latched unless the item had no chunk).
-template <int MAXT, int WB>
+template <int MAXT, int WB, bool GRP>
 __device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, uint32_t* dsm,
                        Control* ec, uint64_t item) {
   using Word = typename WordOf<WB>::T;
   constexpr uint32_t MU = 4u / WB;   // units of a mask
   constexpr uint32_t UPG = 16u / WB; // units of a 16-byte group
   const uint32_t C = a.chunk_elems;
+  const uint32_t group = GRP ? a.group : 1u;
   Word* buf = reinterpret_cast<Word*>(dsm + kCtlWords);
   uint2* wmeta = reinterpret_cast<uint2*>(dsm + kCtlWords + a.meta_offset_words);
   const bool is_chunk = item < a.total_chunks;
@@ -125,12 +136,14 @@ __device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, ui
       }
       ti = lo;
     }
-    c = item - a.chunk_begin[ti];
+    c = (item - a.chunk_begin[ti]) * group;  // the item's first chunk
   } else {
     ti = (uint32_t)(item - a.total_chunks);
   }
   const uint64_t n = ti < a.T ? a.n[ti] : 0;
   const uint64_t nc = ceil_div_u64(n, C);
+  // the item's chunks (1 without grouping)
+  const uint32_t gc = GRP ? (is_chunk ? (uint32_t)min((uint64_t)group, nc - c) : 0u) : 1u;
   auto give_up = [&](uint32_t code) {
     if (code != 0) latch_error(ec, code, item);
     st_release_cta(&ctl.state, 2u);
@@ -176,13 +189,18 @@ __device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, ui
 #pragma unroll
   for (uint32_t j = 0; j < kStreamHeaderWords; ++j) h[j] = sw[j];
   const uint64_t cbeg = c * C;
-  const uint32_t count = is_chunk ? (uint32_t)min((uint64_t)C, n - cbeg) : 0u;
+  const uint32_t count =
+      is_chunk ? (uint32_t)min((uint64_t)(GRP ? gc * C : C), n - cbeg) : 0u;
   const uint32_t nwin = (count + kWindow - 1) / kWindow;
   uint64_t start = 0, end = payload;
   if (is_chunk) {
     const uint32_t* ct = sw + kStreamHeaderWords + 2 * c;
     start = get_u64_words(ct);
-    if (c + 1 < nc) end = get_u64_words(ct + 2);
+    if constexpr (GRP) {
+      if (c + gc < nc) end = get_u64_words(ct + 2 * gc);
+    } else {
+      if (c + 1 < nc) end = get_u64_words(ct + 2);
+    }
   }
   ok = (h[0] == kStreamMagic) & (h[1] == (1u | ((uint32_t)WB << 16))) & (h[2] == kWindow) &
        (h[3] == C) &
@@ -233,6 +251,21 @@ __device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, ui
     fills = body > 0 ? 1u : 0u;
   }
   st_release_cta(&ctl.progress, 1u);  // staged: the scatterer may read the piece
+  // The table entries of the item's inner chunks: where each must start, in units from the
+  // item's start (an entry outside the item or off a unit boundary can match no window).
+  uint32_t* bnd = dsm + kCtlWords + a.meta_offset_words + 2 * (group * C / kWindow);
+  if constexpr (GRP) {
+    const uint32_t* ct = sw + kStreamHeaderWords + 2 * c;
+    uint64_t x[kMaxGroup - 1];
+#pragma unroll
+    for (uint32_t j = 1; j < kMaxGroup; ++j) x[j - 1] = j < gc ? get_u64_words(ct + 2 * j) : 0;
+#pragma unroll
+    for (uint32_t j = 1; j < kMaxGroup; ++j)
+      if (j < gc)
+        bnd[j - 1] = (x[j - 1] >= start && x[j - 1] <= end && (x[j - 1] & (uint64_t)(WB - 1)) == 0)
+                         ? (uint32_t)((x[j - 1] - start) / WB)
+                         : 0xFFFFFFFFu;
+  }
 
   // ---- walk the masks. The chain position -> mask -> next position is the critical
   // path. A window spans at most 33 words, so from buffer position bp the next
@@ -251,6 +284,21 @@ __device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, ui
   unsigned long long* wm = reinterpret_cast<unsigned long long*>(wmeta);
   uint32_t s = 0, bp = ph, m = 0, w = 0, piece = 1;
   bool good = true;
+  // Each inner chunk of the item must start exactly where the walk reaches its first window
+  // (the chunk table's rule). Checked after every step, from the window table (or, for the
+  // window walked next, bp), while the positions still refer to the current piece.
+  const uint32_t wpc = C / kWindow;
+  uint32_t jb = 1, nb = wpc;  // the next inner chunk and its first window
+  auto check_bounds = [&]() {
+    if constexpr (GRP) {
+      while (jb < gc && nb <= w) {
+        const uint32_t at = nb < w ? (uint32_t)wm[nb] - MU : bp;
+        good = good && s + (at - ph) == bnd[jb - 1];
+        ++jb;
+        nb += wpc;
+      }
+    }
+  };
   // the mask at unit p (for WB = 2 it may sit on a 2-byte boundary: two 16-bit loads)
   auto mask_at = [&](uint32_t p) -> uint32_t {
     if (WB == 4) return (uint32_t)buf[p];
@@ -266,6 +314,7 @@ __device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, ui
         wm[w] = (unsigned long long)(bp + MU) | ((unsigned long long)m << 32);
         bp += MU + __popc(m);
       }
+      check_bounds();
       continue;
     }
     if (bp + MU <= cap) {
@@ -275,6 +324,7 @@ __device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, ui
         wm[w] = (unsigned long long)(bp + MU) | ((unsigned long long)m << 32);
         bp = nb;
         ++w;
+        check_bounds();
         continue;
       }
     }
@@ -336,7 +386,7 @@ __device__ void walker(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, ui
 }
 
 // Warp 1: expands the recorded windows of its chunk as the walker records them.
-template <int MAXT, int WB>
+template <int MAXT, int WB, bool GRP>
 __device__ void scatterer(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl, uint32_t* dsm,
                           Control* ec, uint64_t item, uint32_t lane) {
   if (item >= a.total_chunks) return;  // header checks only: the walker does them
@@ -350,9 +400,9 @@ __device__ void scatterer(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl,
     }
     ti = lo;
   }
-  const uint64_t c = item - a.chunk_begin[ti];
+  const uint64_t c = GRP ? (item - a.chunk_begin[ti]) * a.group : item - a.chunk_begin[ti];
   const uint64_t cbeg = c * C;
-  const uint32_t count = (uint32_t)min((uint64_t)C, a.n[ti] - cbeg);
+  const uint32_t count = (uint32_t)min((uint64_t)(GRP ? a.group * C : C), a.n[ti] - cbeg);
   using Word = typename WordOf<WB>::T;
   constexpr uint32_t EPL = 16u / WB;       // units a lane expands: one 16-byte store
   constexpr uint32_t LPW = kWindow / EPL;  // lanes per window: 8 (WB = 4) or 4 (WB = 2)
@@ -466,8 +516,15 @@ __device__ void scatterer(const DecompressArgs<MAXT, WB>& a, DecompressCtl& ctl,
   }
 }
 
-// Every chunk gets a scatterer warp of its own and a lane of the CTA's walker warp; the
-// host picks the chunks per CTA and the chunk buffer's size (zvc_plan.h).
+// Chunks per work item: 1 from 4096 elements on, else up to kMaxGroup chunks of up to 4096
+// elements in all (measured: at C = 1024 sparse maps decode at 0.61-0.66 of HBM one chunk
+// per item, as C = 4096 chunks do at 0.88-0.97).
+__host__ __device__ inline uint32_t group_of(uint32_t C) {
+  return C >= kTileElems ? 1u : min(kMaxGroup, kTileElems / C);
+}
+
+// Every item gets a scatterer warp of its own and a lane of the CTA's walker warp; the
+// host picks the items per CTA and the buffer's size (zvc_plan.h).
 constexpr uint32_t kMaxThreads = 32 * (1 + plan::kMaxChunksPerCta);
 // Chunks of at most 1024 elements are bound by the chunks in flight per SM, which registers
 // limit: their kernel is built for 10 CTAs of kMaxThreads per SM (32 registers; measured
@@ -475,7 +532,7 @@ constexpr uint32_t kMaxThreads = 32 * (1 + plan::kMaxChunksPerCta);
 constexpr uint32_t kSmallChunkElems = 1024;
 constexpr uint32_t kSmallMinCtas = 10;
 
-template <int MAXT, int WB, bool SMALL>
+template <int MAXT, int WB, bool SMALL, bool GRP>
 __global__ void __launch_bounds__(kMaxThreads, SMALL ? kSmallMinCtas : 0)
     decompress_kernel(const __grid_constant__ DecompressArgs<MAXT, WB> a) {
   extern __shared__ __align__(16) uint32_t dsm_all[];
@@ -500,14 +557,16 @@ __global__ void __launch_bounds__(kMaxThreads, SMALL ? kSmallMinCtas : 0)
   // the window tables start cleared: an entry is taken once it reads non-zero
   for (uint32_t c2 = 0; c2 < a.chunks_per_cta; ++c2) {
     uint32_t* wz = dsm_all + (uint64_t)c2 * a.slot_words + kCtlWords + a.meta_offset_words;
-    for (uint32_t i = threadIdx.x; i < 2u * (a.chunk_elems / kWindow); i += blockDim.x) wz[i] = 0u;
+    for (uint32_t i = threadIdx.x; i < 2u * ((GRP ? a.group : 1u) * a.chunk_elems / kWindow);
+         i += blockDim.x)
+      wz[i] = 0u;
   }
   __syncthreads();
   if (warp == 0) {
-    if (lane < a.chunks_per_cta && item < a.total_items) walker(a, ctl, dsm, ec, item);
+    if (lane < a.chunks_per_cta && item < a.total_items) walker<MAXT, WB, GRP>(a, ctl, dsm, ec, item);
   } else {
     if (item >= a.total_items) return;
-    scatterer(a, ctl, dsm, ec, item, lane);
+    scatterer<MAXT, WB, GRP>(a, ctl, dsm, ec, item, lane);
   }
 }
 
@@ -541,7 +600,7 @@ zvc_status device_limits(plan::Limits* d) {
   return ZVC_OK;
 }
 
-template <int MAXT, int WB, bool SMALL>
+template <int MAXT, int WB, bool SMALL, bool GRP>
 zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, uint32_t T,
                     bool batched, uint32_t C, uint8_t* ws, cudaStream_t stream) {
   static_assert(WB == 4 || MAXT == 1, "16-bit words: single streams only");
@@ -551,31 +610,35 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   args.ws = ws;
   args.wait_limit_ns = kDefaultWaitLimitNs;
   args.chunk_elems = C;
+  args.group = GRP ? group_of(C) : 1u;
   args.T = T;
   args.batched = batched ? 1u : 0u;
-  uint64_t chunks = 0;
+  const uint32_t IC = args.group * C;  // elements of a whole work item
+  uint64_t chunks = 0, table_chunks = 0;
   for (uint32_t i = 0; i < T; ++i) {
     args.out[i] = static_cast<typename WordOf<WB>::T*>(ts[i].ptr);
     args.n[i] = ts[i].n;
     args.chunk_begin[i] = chunks;
-    chunks += ceil_div_u64(ts[i].n, C);
+    chunks += ceil_div_u64(ceil_div_u64(ts[i].n, C), args.group);
+    table_chunks += ceil_div_u64(ts[i].n, C);
   }
   args.chunk_begin[T] = chunks;
   args.total_chunks = chunks;
   args.total_items = chunks + (batched && T == 0 ? 1 : T);
-  const uint32_t wpc = C / kWindow;
-  const uint32_t full_cap = plan::full_cap_words(C, WB);
+  const uint32_t wpc = IC / kWindow;  // windows of a whole work item
+  const uint32_t full_cap = plan::full_cap_words(IC, WB);
   plan::Limits d;
   zvc_status st = device_limits(&d);
   if (st != ZVC_OK) return st;
   // the most shared memory a CTA of this chunk size can ask for (within the device's
   // limit), and all of the SM's unified memory as shared memory
-  const uint64_t most = plan::slot_bytes(full_cap, C) * plan::kMaxChunksPerCta;
+  const uint32_t extra = GRP ? kBndWords : 0u;  // the inner chunks' starts
+  const uint64_t most = plan::slot_bytes(full_cap, IC, extra) * plan::kMaxChunksPerCta;
   cudaError_t e = cudaFuncSetAttribute(
-      decompress_kernel<MAXT, WB, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      decompress_kernel<MAXT, WB, SMALL, GRP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)min(most, (uint64_t)d.smem_per_cta_max));
   if (e != cudaSuccess) return cuda_failure(e);
-  e = cudaFuncSetAttribute(decompress_kernel<MAXT, WB, SMALL>,
+  e = cudaFuncSetAttribute(decompress_kernel<MAXT, WB, SMALL, GRP>,
                            cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return cuda_failure(e);
   // the buffer's size and the chunks per CTA, with the occupancy the runtime reports
@@ -583,8 +646,8 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
   auto occ = [&](uint32_t k, uint32_t cap) -> int {
     int n = 0;
     const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &n, decompress_kernel<MAXT, WB, SMALL>, (int)(32 * (1 + k)),
-        (size_t)(k * plan::slot_bytes(cap, C)));
+        &n, decompress_kernel<MAXT, WB, SMALL, GRP>, (int)(32 * (1 + k)),
+        (size_t)(k * plan::slot_bytes(cap, IC, extra)));
     if (r != cudaSuccess) {
       occ_err = r;
       return -1;
@@ -592,17 +655,18 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
     return n;
   };
   plan::Plan pl;
-  if (!plan::decompress_plan(chunks, in_bytes, T, batched, C, d, occ, &pl, WB))
+  if (!plan::decompress_plan(chunks, in_bytes, T, batched, IC, d, occ, &pl, WB,
+                             table_chunks, extra))
     return cuda_failure(occ_err);
   args.cap_words = pl.cap_words;
   args.chunks_per_cta = pl.chunks_per_cta;
   args.meta_offset_words = args.cap_words;
-  args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.cap_words + 2ull * wpc, 4);
+  args.slot_words = (uint32_t)round_up_u64(kCtlWords + args.cap_words + 2ull * wpc + extra, 4);
   const uint64_t smem = 4ull * args.slot_words * args.chunks_per_cta;
   const uint32_t threads = 32u * (1u + args.chunks_per_cta);
   const uint64_t blocks = ceil_div_u64(args.total_items, args.chunks_per_cta);
   const TraceMark mark = trace_begin(kTraceDecompress, stream);
-  decompress_kernel<MAXT, WB, SMALL><<<(unsigned)blocks, threads, smem, stream>>>(args);
+  decompress_kernel<MAXT, WB, SMALL, GRP><<<(unsigned)blocks, threads, smem, stream>>>(args);
   trace_end(mark, stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_failure(e);
@@ -612,9 +676,12 @@ zvc_status launch_k(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, 
 template <int MAXT, int WB>
 zvc_status launch_t(const uint32_t* in, uint64_t in_bytes, const TensorOut* ts, uint32_t T,
                     bool batched, uint32_t C, uint8_t* ws, cudaStream_t stream) {
-  if (C <= kSmallChunkElems)
-    return launch_k<MAXT, WB, true>(in, in_bytes, ts, T, batched, C, ws, stream);
-  return launch_k<MAXT, WB, false>(in, in_bytes, ts, T, batched, C, ws, stream);
+  const bool grp = group_of(C) > 1;
+  const bool small = group_of(C) * C <= kSmallChunkElems;
+  if (grp && small) return launch_k<MAXT, WB, true, true>(in, in_bytes, ts, T, batched, C, ws, stream);
+  if (grp) return launch_k<MAXT, WB, false, true>(in, in_bytes, ts, T, batched, C, ws, stream);
+  if (small) return launch_k<MAXT, WB, true, false>(in, in_bytes, ts, T, batched, C, ws, stream);
+  return launch_k<MAXT, WB, false, false>(in, in_bytes, ts, T, batched, C, ws, stream);
 }
 
 }  // namespace

@@ -41,16 +41,19 @@ inline uint32_t full_cap_words(uint32_t C, uint32_t wb = 4) {
   return (uint32_t)round_up4((uint64_t)C / kWindowWords + C + 3);
 }
 
-// Shared memory of one chunk's slot whose buffer holds cap words.
-inline uint64_t slot_bytes(uint32_t cap, uint32_t C) {
-  return 4ull * round_up4(kSlotCtlWords + (uint64_t)cap + 2ull * (C / kWindowWords));
+// Shared memory of one chunk's slot whose buffer holds cap words (and `extra` words more).
+inline uint64_t slot_bytes(uint32_t cap, uint32_t C, uint32_t extra = 0) {
+  return 4ull * round_up4(kSlotCtlWords + (uint64_t)cap + 2ull * (C / kWindowWords) + extra);
 }
 
 // The mean chunk in words: the stream's size less its headers (32 bytes per tensor, plus
-// the batch header and table when batched) and chunk tables (8 bytes per chunk).
-inline uint64_t mean_chunk_words(uint64_t in_bytes, uint64_t chunks, uint32_t T, bool batched) {
+// the batch header and table when batched) and chunk tables (8 bytes per table entry; a
+// work item may group several table chunks, table_chunks of them in all).
+inline uint64_t mean_chunk_words(uint64_t in_bytes, uint64_t chunks, uint32_t T, bool batched,
+                                 uint64_t table_chunks = 0) {
+  if (table_chunks < chunks) table_chunks = chunks;
   const uint64_t fixed = (batched ? 16ull + 8ull * ((uint64_t)T + 1) : 0ull) + 32ull * T +
-                         8ull * chunks;
+                         8ull * table_chunks;
   return in_bytes > fixed && chunks > 0 ? (in_bytes - fixed) / 4 / chunks : 0;
 }
 
@@ -71,12 +74,13 @@ inline uint64_t mean_chunk_words(uint64_t in_bytes, uint64_t chunks, uint32_t T,
 //   stages fewer chunks in pieces.
 template <class Occ>
 bool decompress_plan(uint64_t chunks, uint64_t in_bytes, uint32_t T, bool batched, uint32_t C,
-                     const Limits& d, Occ occ, Plan* out, uint32_t wb = 4) {
+                     const Limits& d, Occ occ, Plan* out, uint32_t wb = 4,
+                     uint64_t table_chunks = 0, uint32_t extra = 0) {
   const uint32_t full_cap = full_cap_words(C, wb);
   out->cap_words = full_cap;
   out->chunks_per_cta = 1;
   if (chunks == 0) return true;
-  uint64_t mean = mean_chunk_words(in_bytes, chunks, T, batched);
+  uint64_t mean = mean_chunk_words(in_bytes, chunks, T, batched, table_chunks);
   if (mean > full_cap) mean = full_cap;
   uint64_t want = round_up4(mean * kCapSlackNum / kCapSlackDen + kCapExtraWords);
   if (want < kCapMinWords) want = kCapMinWords;
@@ -90,7 +94,7 @@ bool decompress_plan(uint64_t chunks, uint64_t in_bytes, uint32_t T, bool batche
   const bool waves2 = o1 > 0 && chunks >= 2ull * (uint64_t)o1 * (uint64_t)d.sms;
   uint64_t best = (uint64_t)o1;
   for (uint32_t kk = 2; short_chunks && waves2 && kk <= kMaxChunksPerCta; kk *= 2) {
-    if (kk * slot_bytes(cap, C) > (uint64_t)d.smem_per_cta_max) break;
+    if (kk * slot_bytes(cap, C, extra) > (uint64_t)d.smem_per_cta_max) break;
     const int o = occ(kk, cap);
     if (o < 0) return false;
     if (o > 0 && (uint64_t)o * kk >= best) {
@@ -110,7 +114,7 @@ bool decompress_plan(uint64_t chunks, uint64_t in_bytes, uint32_t T, bool batche
   const uint64_t cta_max = (uint64_t)d.smem_per_cta_max + (uint64_t)d.reserved_per_cta;
   if (per_cta > cta_max) per_cta = cta_max;
   const uint64_t fixed = (uint64_t)d.reserved_per_cta +
-                         4ull * k * (kSlotCtlWords + round_up4(2ull * (C / kWindowWords)));
+                         4ull * k * (kSlotCtlWords + round_up4(2ull * (C / kWindowWords) + extra));
   if (per_cta <= fixed + 16ull * k) return true;
   uint64_t c = ((per_cta - fixed) / (4ull * k)) & ~3ull;
   if (c > full_cap) c = full_cap;
