@@ -19,6 +19,9 @@ constexpr uint32_t kSlotCtlWords = 8;        // control words at the head of a s
 // 31 windows), at most the largest valid chunk.
 constexpr uint64_t kCapSlackNum = 5, kCapSlackDen = 4, kCapExtraWords = 64;
 constexpr uint32_t kCapMinWords = 1024;
+// ... and at most a dense 4096-element chunk's words (with its phase): longer chunks (C above
+// 4096) go in pieces rather than holding so much shared memory that only a few are in flight.
+constexpr uint32_t kCapMaxWords = 4240;
 constexpr uint32_t kMaxChunksPerCta = 4;     // chunks one walker warp walks at once
 constexpr uint64_t kMultiMeanDiv = 6;        // several chunks per CTA: mean <= largest / 6,
 constexpr uint32_t kMultiAnyWords = 1060;    // or chunks of at most 1024 elements
@@ -84,6 +87,7 @@ bool decompress_plan(uint64_t chunks, uint64_t in_bytes, uint32_t T, bool batche
   if (mean > full_cap) mean = full_cap;
   uint64_t want = round_up4(mean * kCapSlackNum / kCapSlackDen + kCapExtraWords);
   if (want < kCapMinWords) want = kCapMinWords;
+  if (want > kCapMaxWords) want = kCapMaxWords;
   uint32_t cap = want < full_cap ? (uint32_t)want : full_cap;
 
   int o1 = occ(1u, cap);
