@@ -340,6 +340,9 @@ __device__ void pack_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& s
   const unsigned long long G = gridDim.x;
   const uint32_t lane_below = (1u << lane) - 1u;
   const bool keep_woff = a.inner_chunks != 0;
+  // window offsets of every window, or (chunks of a multiple of 512 elements, whose starts
+  // fall on warps' first windows) of each warp's first window only
+  const bool woff_each = keep_woff && a.chunk_elems % (kWinPerWarp * kWindow) != 0;
   const uint32_t w0 = q * kWinPerWarp;  // this warp's first window
   uint32_t round = 0;
   for (uint32_t i = team;; i += kTeams, ++round) {
@@ -407,9 +410,11 @@ __device__ void pack_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& s
     uint32_t* woff = sm.woff[s] + w0;
     // (the order of these branches is measured: with the plain loop first the 5-25% maps
     // gain 2% and the 0-1% ones lose 4-6%, which leaves every density above 0.7 of HBM)
-    if (nwin == kTileWindows && !keep_woff && nzw > kSkipBelow && nzw < kSkipAbove) {
+    // chunks of a multiple of 512 elements start only at a warp's first window: its base
+    if (keep_woff && lane == 0) woff[0] = pos;
+    if (nwin == kTileWindows && !woff_each && nzw > kSkipBelow && nzw < kSkipAbove) {
       pack_whole<WB, false, false>(sa, pos, v, m, lane, lane_below, woff);
-    } else if (nwin == kTileWindows && !keep_woff) {
+    } else if (nwin == kTileWindows && !woff_each) {
       pack_whole<WB, true, false>(sa, pos, v, m, lane, lane_below, woff);
     } else if (nwin == kTileWindows) {  // chunks start inside tiles: window offsets are kept
       // one loop only: every unrolled copy of the loop in this kernel slows all of them

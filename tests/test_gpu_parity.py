@@ -51,7 +51,7 @@ SIZES = [1, 2, 31, 32, 33, 127, 128, 129, 4095, 4096, 4097, 8191, 8192, 12_293, 
          100_003, 1_000_003]
 
 
-@pytest.mark.parametrize("C", [32, 64, 96, 1024, 4096, 16384, 32768])
+@pytest.mark.parametrize("C", [32, 64, 96, 128, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768])
 def test_random_ragged_sizes(C):
     rng = np.random.default_rng(C)
     for n in SIZES:
