@@ -174,3 +174,67 @@ def test_offload_and_prefetch_from_two_threads_at_once():
         assert np.array_equal(h[:size].numpy(), ref)
     for y in ys:
         assert torch.equal(y, xb.view(torch.int32))
+
+
+def test_offload_of_more_segments_than_staging_buffers():
+    """Five segments through three staging buffers, each reused: the batch equals the
+    oracle's and restores bit for bit, and a second offload through the same workspace
+    gives the same bytes."""
+    C = 4096
+    n = 4 * (1 << 25) + 12_345
+    x = workloads.odd_case(n, device="cuda", density=0.1)[0]
+    h, size, ws = _offload(x, C)
+    seg = zvc.zvc_offload_segment_elems(n, C)
+    assert -(-n // seg) == 5
+    w = words_of(x)
+    ref = oracle.encode_batch([w[k:k + seg] for k in range(0, n, seg)], C)
+    assert size == ref.size
+    assert np.array_equal(h[:size].numpy(), ref)
+    y = _prefetch(h, size, n, C, ws)
+    assert torch.equal(y, x.view(torch.int32))
+    h2, size2, _ = _offload(x, C)
+    assert size2 == size and torch.equal(h2[:size], h[:size])
+
+
+@pytest.mark.parametrize("shift", [8, 16, 24])
+def test_offload_and_prefetch_through_a_host_base_off_16_bytes(shift):
+    """A host buffer at any 8-byte aligned base: the batch lands exactly in place and
+    restores, and nothing outside it is written."""
+    ensure_lib()
+    C = 1024
+    n = 2_000_003
+    x = workloads.odd_case(n, device="cuda", density=0.45)[0]
+    cap = zvc.zvc_offload_host_bound(n, C)
+    buf = torch.full((cap + 64,), 0xAB, dtype=torch.uint8, pin_memory=True)
+    ws = zvc.new_workspace(zvc.zvc_offload_workspace_size(n, C))
+    st, size = zvc.zvc_offload(x.data_ptr(), n, C, buf.data_ptr() + shift, cap, ws.data_ptr(),
+                               ws.numel(), sh())
+    assert st == zvc.ZVC_OK
+    assert zvc.zvc_offload_join(sh()) == zvc.ZVC_OK  # the copies, on the library's stream
+    assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+    host = buf.numpy()
+    assert (host[:shift] == 0xAB).all() and (host[shift + size:] == 0xAB).all()
+    ref = oracle.encode_batch([words_of(x)], C)
+    assert np.array_equal(host[shift:shift + size], ref)
+    y = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+    assert zvc.zvc_prefetch(buf.data_ptr() + shift, size, y.data_ptr(), n, C, ws.data_ptr(),
+                            ws.numel(), sh()) == zvc.ZVC_OK
+    assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+    assert torch.equal(y, x.view(torch.int32))
+
+
+def test_prefetch_from_pageable_host_memory():
+    """A batch in ordinary (pageable) host memory restores too, at either 8-byte phase."""
+    C = 4096
+    n = 40_000_003  # two segments
+    x = workloads.odd_case(n, device="cuda", density=0.3)[0]
+    h, size, ws = _offload(x, C)
+    pageable = torch.empty(size + 4, dtype=torch.uint8)
+    assert not pageable.is_pinned()
+    for off in (0, 4):
+        pageable[off:off + size] = h[:size]
+        y = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+        assert zvc.zvc_prefetch(pageable.data_ptr() + off, size, y.data_ptr(), n, C,
+                                ws.data_ptr(), ws.numel(), sh()) == zvc.ZVC_OK
+        assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+        assert torch.equal(y, x.view(torch.int32))
