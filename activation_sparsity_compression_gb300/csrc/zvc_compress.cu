@@ -48,7 +48,7 @@ struct CompressArgs {
   uint8_t* ws;
   uint64_t total_tiles;
   uint64_t wait_limit_ns;
-  uint64_t epoch;          // tags this launch's entries in the workspace
+  uint64_t epoch;          // tags this launch's entries in the workspace (host-drawn)
   uint64_t hdr_words_end;  // batch prefix + every stream's header and table, in units
   uint32_t chunk_elems;
   uint32_t T;
@@ -119,6 +119,8 @@ struct __align__(16) CompressShared {
   uint32_t incl_ti[2];   // ... and its tensor, and that tensor's start in the payload
   uint64_t incl_pstart[2];
   uint64_t pbuf[ZVC_MAX_BATCH + 1];  // stream starts, for the headers
+  uint64_t epoch;                    // a captured launch's epoch, read at its start
+  uint64_t epoch_bar;                // completes once `epoch` is set (captured launches)
 };
 
 static_assert(sizeof(CompressShared<4>) <= 227 * 1024, "one CTA per SM must fit");
@@ -169,12 +171,13 @@ __device__ __forceinline__ void fill_slot(const CompressArgs<MAXT, WB>& a, Compr
 // A tensor's start in the payload, published by its first tile in this launch (bounded
 // wait); false if that tile gave up or the wait ran out.
 template <int MAXT, int WB>
-__device__ bool wait_tensor_start(const CompressArgs<MAXT, WB>& a, const TensorStart* ts, Control* ctl,
-                                  uint64_t info, uint64_t* value) {
+__device__ bool wait_tensor_start(const CompressArgs<MAXT, WB>& a, uint64_t epoch,
+                                  const TensorStart* ts, Control* ctl, uint64_t info,
+                                  uint64_t* value) {
   WaitClock clock;
   while (true) {
     const uint64_t tag = ld_acquire_u64(&ts->tag);
-    if ((tag >> 2) == a.epoch) {
+    if ((tag >> 2) == epoch) {
       if ((tag & 3u) == kStartPrefix) {
         *value = ld_relaxed_u64(&ts->value);
         return true;
@@ -188,9 +191,9 @@ __device__ bool wait_tensor_start(const CompressArgs<MAXT, WB>& a, const TensorS
 }
 
 template <int MAXT, int WB>
-__device__ void finalize_warp(const CompressArgs<MAXT, WB>& a, uint64_t total_payload, bool failed,
-                              const TensorStart* tstart, Control* ctl, uint64_t* pbuf,
-                              uint32_t lane) {
+__device__ void finalize_warp(const CompressArgs<MAXT, WB>& a, uint64_t epoch,
+                              uint64_t total_payload, bool failed, const TensorStart* tstart,
+                              Control* ctl, uint64_t* pbuf, uint32_t lane) {
   int bad = failed;
   if (lane == 0) {
     // pbuf[i] = payload words before stream i; an empty tensor starts where the next
@@ -202,7 +205,7 @@ __device__ void finalize_warp(const CompressArgs<MAXT, WB>& a, uint64_t total_pa
       uint64_t p = next;
       if (a.tile_begin[i + 1] > a.tile_begin[i]) {
         p = 0;
-        if (MAXT > 1 && !wait_tensor_start(a, tstart + i, ctl, a.total_tiles, &p)) bad = 1;
+        if (MAXT > 1 && !wait_tensor_start(a, epoch, tstart + i, ctl, a.total_tiles, &p)) bad = 1;
       }
       pbuf[i] = p;
       next = p;
@@ -235,6 +238,19 @@ __device__ void finalize_warp(const CompressArgs<MAXT, WB>& a, uint64_t total_pa
     }
     if (a.out_size) *a.out_size = total_bytes;
   }
+}
+
+// ---- epochs. A launch outside a stream capture tags its workspace entries with the epoch
+// the host drew for it (CompressArgs::epoch: a process-wide counter started between 2^39
+// and 2^40). A launch captured in a CUDA graph is replayed with the arguments of its
+// capture, so it reads its epoch on the device instead: one more than the workspace's
+// epoch counter, read by every CTA at its start (by a store warp, idle until the first
+// tile is settled) and moved on once every CTA has read it (settle_role, tile G - 1). Its
+// epochs are 1, 2, ... in a fresh workspace: never the 0 of an unwritten status word,
+// never a host-drawn epoch, and a new one on every replay.
+template <bool CAPTURED, int MAXT, int WB>
+__device__ __forceinline__ uint64_t launch_epoch(const CompressArgs<MAXT, WB>& a, uint64_t dev) {
+  return CAPTURED ? dev : a.epoch;
 }
 
 // ---- pack teams
@@ -334,7 +350,7 @@ __device__ __forceinline__ void pack_whole(uint32_t slot_addr, uint32_t pos,
 constexpr uint32_t kSkipBelow = 16;
 constexpr uint32_t kSkipAbove = 320;
 
-template <int MAXT, int WB, bool INNER>
+template <int MAXT, int WB, bool INNER, bool CAPTURED>
 __device__ void pack_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& sm, uint64_t* status,
                           Control* ctl, uint32_t team, uint32_t q, uint32_t lane) {
   const unsigned long long G = gridDim.x;
@@ -344,13 +360,22 @@ __device__ void pack_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& s
   // fall on warps' first windows) of each warp's first window only
   const bool woff_each = keep_woff && a.chunk_elems % (kWinPerWarp * kWindow) != 0;
   const uint32_t w0 = q * kWinPerWarp;  // this warp's first window
+  // a captured launch: the team's first warp, which publishes the aggregates, waits for
+  // the epoch first (a wait that runs out makes it late for its first tile, so the team
+  // gives the tile up together)
+  uint64_t dev_epoch = 0;
+  bool epoch_ok = true;
+  if (CAPTURED && q == 0) {
+    epoch_ok = mbar_wait(&sm.epoch_bar, 0u, a.wait_limit_ns);
+    dev_epoch = sm.epoch;
+  }
   uint32_t round = 0;
   for (uint32_t i = team;; i += kTeams, ++round) {
     const unsigned long long t = blockIdx.x + (unsigned long long)i * G;
     if (t >= a.total_tiles) return;
     const int s = (int)(i % kSlots);
     // a warp whose wait ran out reads nothing; the team learns of it at its barrier below
-    const bool late = !mbar_wait(&sm.full[s], (i / kSlots) & 1u, a.wait_limit_ns);
+    const bool late = !mbar_wait(&sm.full[s], (i / kSlots) & 1u, a.wait_limit_ns) || !epoch_ok;
     const SlotInfo& f = sm.info[s];
     uint32_t* slot = sm.slot[s];
     // read: this lane's word of each of the warp's 16 windows
@@ -400,7 +425,8 @@ __device__ void pack_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& s
     const uint32_t agg = __reduce_add_sync(0xffffffffu, x);
     uint32_t pos = pos0;
     if (q == 0 && lane == 0) {
-      st_relaxed_u64(status + t, (a.epoch << kAggBits) | agg);  // publish the aggregate now
+      // publish the aggregate now
+      st_relaxed_u64(status + t, (launch_epoch<CAPTURED>(a, dev_epoch) << kAggBits) | agg);
       sm.info[s].agg = agg;
     }
     // write back, packed (a store of the non-zero words and one of the mask per window,
@@ -439,16 +465,27 @@ __device__ void pack_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& s
 // ahead: no settle waits for another CTA's settle. Two warps take alternate tiles; each
 // sums its window on its own and then adds the previous tile's inclusive prefix, handed
 // over through shared memory.
-template <int MAXT, int WB>
+template <int MAXT, int WB, bool CAPTURED>
 __device__ void settle_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& sm, const uint64_t* status,
                             TensorStart* tstart, Control* ctl, uint32_t k, uint32_t lane) {
   const unsigned long long G = gridDim.x;
   uint64_t lb[kLookbackWidth];
   uint32_t i = k;
   unsigned long long t = blockIdx.x + k * G;
+  // (the entries a pass holds below its floor are never read, so a captured launch's
+  // first pass goes out before its epoch is known)
   if (t < a.total_tiles)
-    aggsum_issue<kLookbackWidth>(status, a.epoch, (int64_t)t - 1, i ? (int64_t)(t - G) : -1,
-                                 lane, lb);
+    aggsum_issue<kLookbackWidth>(status, launch_epoch<CAPTURED>(a, 0), (int64_t)t - 1,
+                                 i ? (int64_t)(t - G) : -1, lane, lb);
+  uint64_t dev_epoch = 0;
+  if (CAPTURED) {
+    if (!mbar_wait(&sm.epoch_bar, 0u, a.wait_limit_ns)) {
+      if (lane == 0) latch_error(ctl, ZVC_ERR_TIMEOUT, t);
+      return;
+    }
+    dev_epoch = sm.epoch;
+  }
+  const uint64_t epoch = launch_epoch<CAPTURED>(a, dev_epoch);
   for (; t < a.total_tiles; i += 2, t += 2 * G) {
     const int s = (int)(i % kSlots);
     if (!mbar_wait(&sm.packed[s], (i / kSlots) & 1u, a.wait_limit_ns)) {
@@ -465,14 +502,21 @@ __device__ void settle_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>&
     // tile lies inside this tile's look-back window (t - G, t), and pstart is excl less the
     // aggregates from that first tile on, which the look-back reads anyway. So no tile
     // waits for another CTA's settle.
-    bool ok = MAXT > 1 ? aggsum_finish<kLookbackWidth, true>(status, a.epoch, t, floor, lane,
+    bool ok = MAXT > 1 ? aggsum_finish<kLookbackWidth, true>(status, epoch, t, floor, lane,
                                                              a.wait_limit_ns, ctl, lb, &excl,
                                                              (int64_t)a.tile_begin[ti],
                                                              &since_start)
-                       : aggsum_finish<kLookbackWidth>(status, a.epoch, t, floor, lane,
+                       : aggsum_finish<kLookbackWidth>(status, epoch, t, floor, lane,
                                                        a.wait_limit_ns, ctl, lb, &excl);
+    // A captured launch: tile G - 1 is the last of the first round, and its look-back has
+    // read the aggregates of tiles 0 .. G - 2, one from every other CTA, each tagged with
+    // the epoch that CTA read at its start. So every CTA has read the counter: move it on.
+    // After a timeout some CTA may not have read it yet; the counter then skips a value,
+    // so that such a CTA's entries never carry the next launch's epoch.
+    if (CAPTURED && t + 1 == G && lane == 0)
+      st_relaxed_u64(reinterpret_cast<uint64_t*>(a.ws + kEpochOffset), ok ? epoch : epoch + 1);
     if (t + 2 * G < a.total_tiles)  // start this warp's next pass
-      aggsum_issue<kLookbackWidth>(status, a.epoch, (int64_t)(t + 2 * G) - 1, (int64_t)(t + G),
+      aggsum_issue<kLookbackWidth>(status, epoch, (int64_t)(t + 2 * G) - 1, (int64_t)(t + G),
                                    lane, lb);
     uint32_t prev_ti = ~0u;
     uint64_t prev_pstart = 0;
@@ -505,7 +549,7 @@ __device__ void settle_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>&
     if (lane == 0) {
       if (MAXT > 1 && lt == 0) {  // the headers need every stream's start (finalize_warp)
         st_relaxed_u64(&tstart[ti].value, excl);
-        st_release_u64(&tstart[ti].tag, (a.epoch << 2) | (ok ? kStartPrefix : kStartError));
+        st_release_u64(&tstart[ti].tag, (epoch << 2) | (ok ? kStartPrefix : kStartError));
       }
       f.dst = dst;
       f.excl = excl;
@@ -515,7 +559,7 @@ __device__ void settle_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>&
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (t + 1 == a.total_tiles)  // the last tile: its place gives the total payload
-      finalize_warp(a, ok ? excl + agg : 0, !ok, tstart, ctl, sm.pbuf, lane);
+      finalize_warp(a, epoch, ok ? excl + agg : 0, !ok, tstart, ctl, sm.pbuf, lane);
   }
 }
 
@@ -643,7 +687,7 @@ __device__ void store_role(const CompressArgs<MAXT, WB>& a, CompressShared<WB>& 
   }
 }
 
-template <int MAXT, int WB, bool INNER>
+template <int MAXT, int WB, bool INNER, bool CAPTURED>
 __global__ void __launch_bounds__(kRoleThreads, 1)
     compress_kernel(const __grid_constant__ CompressArgs<MAXT, WB> a) {
   extern __shared__ __align__(16) uint8_t dsmem[];
@@ -655,7 +699,7 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
   const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
 
   if (a.total_tiles == 0) {  // every tensor empty: headers only
-    if (warp == 0) finalize_warp(a, 0, false, tstart, ctl, sm.pbuf, lane);
+    if (warp == 0) finalize_warp(a, 0, 0, false, tstart, ctl, sm.pbuf, lane);
     return;
   }
   if (tid == 0) {
@@ -666,6 +710,7 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     }
     mbar_init(&sm.handoff[0], 1);
     mbar_init(&sm.handoff[1], 1);
+    if (CAPTURED) mbar_init(&sm.epoch_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -676,9 +721,15 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
   if (tid == 0)
     for (int s = 0; s < kFirstFills; ++s) fill_slot(a, sm, s, blockIdx.x + (unsigned long long)s * G);
   if (warp < kSettleWarp0)
-    pack_role<MAXT, WB, INNER>(a, sm, status, ctl, warp / kTeamWarps, warp % kTeamWarps, lane);
-  else if (warp < kStoreWarp0) settle_role(a, sm, status, tstart, ctl, warp - kSettleWarp0, lane);
+    pack_role<MAXT, WB, INNER, CAPTURED>(a, sm, status, ctl, warp / kTeamWarps, warp % kTeamWarps,
+                                         lane);
+  else if (warp < kStoreWarp0)
+    settle_role<MAXT, WB, CAPTURED>(a, sm, status, tstart, ctl, warp - kSettleWarp0, lane);
   else {
+    if (CAPTURED && warp == kStoreWarp0 + 1 && lane == 0) {  // the launch's epoch (see above)
+      sm.epoch = 1u + ld_relaxed_u64(reinterpret_cast<const uint64_t*>(a.ws + kEpochOffset));
+      mbar_arrive(&sm.epoch_bar);
+    }
     if (warp == kStoreWarp0 && lane == 0 && blockIdx.x < a.total_tiles &&
         mbar_wait(&sm.full[0], 0u, a.wait_limit_ns))
       for (int s = kFirstFills; s < kSlots; ++s)
@@ -698,16 +749,18 @@ __global__ void lookback_probe_kernel(uint8_t* ws, uint64_t epoch, uint64_t limi
   aggsum_finish<kLookbackWidth>(status, epoch, 1, -1, threadIdx.x & 31u, limit_ns, ctl, v, &sum);
 }
 
-// Epochs of compress launches: a process-wide counter started at a random point below
-// 2^40, so that entries a previous process may have left in reused device memory do not
-// match either, and far below 2^48, so that it never wraps.
+// Epochs of compress launches outside a stream capture: a process-wide counter started at a
+// random point between 2^39 and 2^40, so that entries a previous process may have left in
+// reused device memory do not match either, so far above the epochs of captured launches
+// (a workspace counter from 1) that the two never meet, and far below 2^48, so that it
+// never wraps.
 std::atomic<uint64_t> g_epoch{0};
 
 uint64_t next_epoch() {
   uint64_t e = g_epoch.load();
   if (e == 0) {
     std::random_device rd;
-    const uint64_t seed = (((uint64_t)rd() << 32) ^ rd()) & ((1ull << 40) - 1);
+    const uint64_t seed = ((((uint64_t)rd() << 32) ^ rd()) & ((1ull << 39) - 1)) | (1ull << 39);
     uint64_t expected = 0;
     g_epoch.compare_exchange_strong(expected, seed | 1);
   }
@@ -718,10 +771,42 @@ uint64_t next_epoch() {
 // WB bytes). Every stream starts on a 4-byte boundary, so that the kernel can write headers
 // and tables as 32-bit words: with WB = 4 every position is one, and WB = 2 is a single
 // stream at `out` (4-byte aligned; checked by the caller).
-template <int MAXT, int WB, bool INNER>
+// CTAs of one compress_kernel instantiation that fit on the current device at once, found
+// once per device. (cudaFuncSetAttribute also loads the kernel, which a launch under stream
+// capture needs done beforehand.)
+template <int MAXT, int WB, bool INNER, bool CAPTURED>
+zvc_status resident_ctas(int dev, int* out) {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> resident_of[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return ZVC_ERR_INVALID_ARG;
+  int resident = resident_of[dev].load();
+  if (resident == 0) {
+    const int smem = (int)sizeof(CompressShared<WB>);
+    cudaError_t e = cudaFuncSetAttribute(compress_kernel<MAXT, WB, INNER, CAPTURED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_failure(e);
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_failure(e);
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+             &per_sm, compress_kernel<MAXT, WB, INNER, CAPTURED>, kRoleThreads, smem)) !=
+        cudaSuccess)
+      return cuda_failure(e);
+    resident = sms * (per_sm > 0 ? per_sm : 1);
+    resident_of[dev].store(resident);
+  }
+  *out = resident;
+  return ZVC_OK;
+}
+
+// Launches compress_kernel over T tensors of WB-byte words into `out` (out_units words of
+// WB bytes). Every stream starts on a 4-byte boundary, so that the kernel can write headers
+// and tables as 32-bit words: with WB = 4 every position is one, and WB = 2 is a single
+// stream at `out` (4-byte aligned; checked by the caller).
+template <int MAXT, int WB, bool INNER, bool CAPTURED>
 zvc_status launch_k(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, void* out,
                     uint64_t out_units, uint64_t* out_size, uint8_t* ws, uint64_t limit_ns,
-                    cudaStream_t stream) {
+                    int dev, cudaStream_t stream) {
   using Word = typename CompressArgs<MAXT, WB>::Word;
   static_assert(WB == 4 || MAXT == 1, "16-bit words: single streams only");
   CompressArgs<MAXT, WB> args;
@@ -730,7 +815,7 @@ zvc_status launch_k(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, vo
   args.out_size = out_size;
   args.ws = ws;
   args.wait_limit_ns = limit_ns;
-  args.epoch = next_epoch();
+  args.epoch = CAPTURED ? 0 : next_epoch();  // a captured launch reads its own on the device
   args.chunk_elems = C;
   args.T = T;
   args.batched = batched ? 1u : 0u;
@@ -751,33 +836,14 @@ zvc_status launch_k(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, vo
   args.total_tiles = tiles;
   args.hdr_words_end = hdr;
 
-  // CTAs of this kernel that fit on the current device at once, found once per device
-  constexpr int kMaxDevices = 64;
-  static std::atomic<int> resident_of[kMaxDevices];
-  const int smem = (int)sizeof(CompressShared<WB>);
-  cudaError_t e;
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_failure(e);
-  if (dev < 0 || dev >= kMaxDevices) return ZVC_ERR_INVALID_ARG;
-  int resident = resident_of[dev].load();
-  if (resident == 0) {
-    e = cudaFuncSetAttribute(compress_kernel<MAXT, WB, INNER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return cuda_failure(e);
-    int sms = 0, per_sm = 0;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return cuda_failure(e);
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel<MAXT, WB, INNER>,
-                                                           kRoleThreads, smem)) != cudaSuccess)
-      return cuda_failure(e);
-    resident = sms * (per_sm > 0 ? per_sm : 1);
-    resident_of[dev].store(resident);
-  }
+  int resident = 0;
+  const zvc_status st = resident_ctas<MAXT, WB, INNER, CAPTURED>(dev, &resident);
+  if (st != ZVC_OK) return st;
   const uint64_t grid = tiles == 0 ? 1 : (tiles < (uint64_t)resident ? tiles : (uint64_t)resident);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kRoleThreads);
-  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.dynamicSmemBytes = sizeof(CompressShared<WB>);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident together
@@ -785,7 +851,7 @@ zvc_status launch_k(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, vo
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const TraceMark mark = trace_begin(kTraceCompress, stream);
-  e = cudaLaunchKernelEx(&cfg, compress_kernel<MAXT, WB, INNER>, args);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, compress_kernel<MAXT, WB, INNER, CAPTURED>, args);
   trace_end(mark, stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_failure(e);
@@ -797,14 +863,35 @@ zvc_status launch_k(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, vo
 // 1-3% faster for it (the kernel's speed depends on its code size: measured on 2^28-word maps
 // and the GoogLeNet batch at C = 4096). The other instantiation keeps its run-time checks,
 // which compile to a faster kernel there than the same code with them folded away.
+// A launch on a capturing stream takes the instantiation that reads its epoch on the device;
+// a launch outside a capture also readies that one, so that a later capture finds it loaded.
+template <int MAXT, int WB, bool INNER>
+zvc_status launch_i(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, void* out,
+                    uint64_t out_units, uint64_t* out_size, uint8_t* ws, uint64_t limit_ns,
+                    cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_failure(e);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return cuda_failure(e);
+  if (cs != cudaStreamCaptureStatusNone)
+    return launch_k<MAXT, WB, INNER, true>(ts, T, batched, C, out, out_units, out_size, ws,
+                                           limit_ns, dev, stream);
+  int r = 0;
+  const zvc_status st = resident_ctas<MAXT, WB, INNER, true>(dev, &r);
+  if (st != ZVC_OK) return st;
+  return launch_k<MAXT, WB, INNER, false>(ts, T, batched, C, out, out_units, out_size, ws,
+                                          limit_ns, dev, stream);
+}
+
 template <int MAXT, int WB>
 zvc_status launch_t(const TensorIn* ts, uint32_t T, bool batched, uint32_t C, void* out,
                     uint64_t out_units, uint64_t* out_size, uint8_t* ws, uint64_t limit_ns,
                     cudaStream_t stream) {
   if (C % kTileElems != 0)
-    return launch_k<MAXT, WB, true>(ts, T, batched, C, out, out_units, out_size, ws, limit_ns,
+    return launch_i<MAXT, WB, true>(ts, T, batched, C, out, out_units, out_size, ws, limit_ns,
                                     stream);
-  return launch_k<MAXT, WB, false>(ts, T, batched, C, out, out_units, out_size, ws, limit_ns,
+  return launch_i<MAXT, WB, false>(ts, T, batched, C, out, out_units, out_size, ws, limit_ns,
                                    stream);
 }
 

@@ -21,17 +21,20 @@ constexpr uint32_t kBatchHeaderWords = 4;       // 16 bytes
 
 // Workspace layout (device memory owned by the caller, 256-byte aligned).
 //   [0, 256)        Control: latched error, persists across calls until zvc_get_error.
-//   [256, 512)      reserved.
+//   [256, 264)      u64 epoch counter of compress launches captured in a CUDA graph.
+//   [264, 512)      reserved.
 //   [512, ...)      u64 tile status[tiles], then TensorStart[T] (compress only).
 // The status entries carry the epoch of the launch that wrote them (a number the host
-// draws anew for every compress launch), so entries left by earlier launches never match
-// and nothing needs clearing between calls.
+// draws anew for every compress launch; a launch captured in a graph reads one more than
+// the workspace's epoch counter and moves the counter on), so entries left by earlier
+// launches never match and nothing needs clearing between calls.
 struct Control {
   uint32_t error;       // first zvc_status latched on the device, 0 if none
   uint32_t pad;
   uint64_t error_info;  // tile or chunk index of that error
 };
 constexpr uint64_t kControlBytes = 256;
+constexpr uint64_t kEpochOffset = 256;
 constexpr uint64_t kStatusOffset = 512;
 
 // Tile status word: the launch's epoch in bits 63..16 and the tile's payload units (an

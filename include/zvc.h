@@ -43,6 +43,13 @@
  *     (corrupt input, a look-back wait that timed out) are latched in the workspace and
  *     reported by zvc_get_error(). The library never traps or aborts a kernel.
  *   - chunk_elems must be a positive multiple of 32 and at most ZVC_MAX_CHUNK_ELEMS.
+ *   - The compress and decompress calls (single, batched, 16-bit, static) may be captured
+ *     in a CUDA graph and replayed. A compress launch tags its workspace entries with an
+ *     epoch of its own; on a capturing stream it takes that epoch from a counter in the
+ *     workspace, on the device, so every replay gets a new one. Make one call of each
+ *     kind before capturing (it loads the kernels and sizes their launches). A replayed
+ *     decompress keeps the in_bytes of its capture. zvc_offload, zvc_prefetch and
+ *     zvc_get_error read or wait on the host and are not for capture.
  */
 #ifndef ZVC_H_
 #define ZVC_H_
