@@ -18,7 +18,8 @@ The same line reports, measured in the same run:
                 in pinned host memory (section V.D: offload and prefetch with
                 cudaMemcpyAsync): H2D of the inputs + zvc_offload (compress, D2H of the
                 compressed segments), then zvc_prefetch (H2D, decompress) + D2H of the
-                restored tensors; the slower direction's uncompressed GB/s
+                restored tensors; the slower direction's uncompressed GB/s, median of the
+                repetitions, beside plain copies of the same bytes taken after each one
   alexnet_stack the offload/prefetch step on the 5-layer AlexNet stack (333 MB) with its
                 host-link figures, and each kernel on those layers
   cpu_baseline  the single-threaded CPU oracle on a bounded sample of the same workload
@@ -664,7 +665,8 @@ def measure_e2e_batch(args, zvc, torch, xs, ys, ns, C, dev, stream):
     zvc_offload (compress, D2H of the compressed segments), then zvc_prefetch (H2D of the
     segments, decompress) and the D2H copy of every restored tensor back into the same
     pinned buffers (a second copy stream). The two directions are timed apart with events
-    on the caller's stream; the value is the slower direction's uncompressed GB/s."""
+    on the caller's stream, each repetition on its own; the value is the slower direction's
+    uncompressed GB/s over the median repetition."""
     sh = stream.cuda_stream
     T = len(xs)
     N = sum(ns)
@@ -716,35 +718,25 @@ def measure_e2e_batch(args, zvc, torch, xs, ys, ns, C, dev, stream):
     for i, (x, y) in enumerate(zip(xs, ys)):
         if not torch.equal(x.view(torch.int32), y.view(torch.int32)):
             raise RuntimeError(f"e2e: tensor {i} is not restored bit-exactly")
-    reps = max(3, min(args.steps, 5))
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
-    barrier()
-    torch.cuda.synchronize(dev)
-    for m in marks:
-        m[0].record(stream)
-        offload_dir()
-        m[1].record(stream)
-        prefetch_dir()
-        m[2].record(stream)
-    torch.cuda.synchronize(dev)
-    ok(zvc.zvc_get_error(ows.data_ptr(), sh), "e2e")
-    for i, (h, x) in enumerate(zip(hx, xs)):
-        if not torch.equal(h.view(torch.int32), x.view(-1).view(torch.int32).cpu()):
-            raise RuntimeError(f"e2e: host tensor {i} is not restored bit-exactly")
-    t_in = reduce_max(sum(m[0].elapsed_time(m[1]) for m in marks), dev)
-    t_out = reduce_max(sum(m[1].elapsed_time(m[2]) for m in marks), dev)
     _, world, _ = dist_env()
     segs = [-(-n // zvc.zvc_offload_segment_elems(n, C)) for n in ns]
     link = sum(h - (16 + 8 * (k + 1)) for h, k in zip(hs, segs))  # segment streams moved
-    off_gbs = whole_job_gbs(4 * N, world, reps, t_in)
-    pre_gbs = whole_job_gbs(4 * N, world, reps, t_out)
 
     # The floor each direction has on this host link: plain copies of the same bytes, the
     # two ways at once as in the step (offload: the inputs in, the compressed bytes out;
     # prefetch: the compressed bytes in, the restored tensors out), with no kernel between.
-    # They overwrite the host streams, so they run after the step has been checked.
+    # It is taken right after each repetition of the step, so that both see the same load
+    # on the host link (the link is shared with the machine's other GPUs and their jobs,
+    # whose traffic comes and goes). The floor's copies overwrite the host streams and the
+    # device inputs, which the next repetition writes again before it reads them, and copy
+    # the restored tensors back over the host inputs, which they equal.
     yb = [y.view(-1).view(torch.uint8) for y in ys]
     xb = [x.view(torch.uint8) for x in dx]
+    kb = [min(h, 4 * n) for h, n in zip(hs, ns)]  # the compressed bytes (of a device buffer)
+    off_pairs = ([(dx[i], hx[i]) for i in range(T)],
+                 [(hb[i][:kb[i]], yb[i][:kb[i]]) for i in range(T)])
+    pre_pairs = ([(xb[i][:kb[i]], hb[i][:kb[i]]) for i in range(T)],
+                 [(hx[i], ys[i].view(-1)) for i in range(T)])
 
     def floor_ms(h2d, d2h):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -760,27 +752,52 @@ def measure_e2e_batch(args, zvc, torch, xs, ys, ns, C, dev, stream):
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1)
 
-    kb = [min(h, 4 * n) for h, n in zip(hs, ns)]  # the compressed bytes (of a device buffer)
-    off_pairs = ([(dx[i], hx[i]) for i in range(T)],
-                 [(hb[i][:kb[i]], yb[i][:kb[i]]) for i in range(T)])
-    pre_pairs = ([(xb[i][:kb[i]], hb[i][:kb[i]]) for i in range(T)],
-                 [(hx[i], ys[i].view(-1)) for i in range(T)])
-    floor_ms(*off_pairs)
-    f_in = reduce_max(min(floor_ms(*off_pairs) for _ in range(reps)), dev)
-    f_out = reduce_max(min(floor_ms(*pre_pairs) for _ in range(reps)), dev)
-    off_floor = whole_job_gbs(4 * N, world, 1, f_in)
-    pre_floor = whole_job_gbs(4 * N, world, 1, f_out)
+    reps = max(5, min(args.steps, 9))
+    t_in, t_out, f_in, f_out = [], [], [], []
+    barrier()
+    torch.cuda.synchronize(dev)
+    for _ in range(reps):
+        m = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        m[0].record(stream)
+        offload_dir()
+        m[1].record(stream)
+        prefetch_dir()
+        m[2].record(stream)
+        torch.cuda.synchronize(dev)
+        t_in.append(m[0].elapsed_time(m[1]))
+        t_out.append(m[1].elapsed_time(m[2]))
+        ok(zvc.zvc_get_error(ows.data_ptr(), sh), "e2e")
+        for i, (x, y) in enumerate(zip(xs, ys)):
+            if not torch.equal(x.view(torch.int32), y.view(torch.int32)):
+                raise RuntimeError(f"e2e: tensor {i} is not restored bit-exactly")
+        f_in.append(floor_ms(*off_pairs))
+        f_out.append(floor_ms(*pre_pairs))
+    for i, (h, x) in enumerate(zip(hx, xs)):  # the host copies, once
+        if not torch.equal(h.view(torch.int32), x.view(-1).view(torch.int32).cpu()):
+            raise RuntimeError(f"e2e: host tensor {i} is not restored bit-exactly")
+
+    def gbs(ms):  # uncompressed GB/s of one step that took ms
+        return whole_job_gbs(4 * N, world, 1, reduce_max(ms, dev))
+
+    med = statistics.median
+    off_gbs, pre_gbs = gbs(med(t_in)), gbs(med(t_out))
+    off_floor, pre_floor = gbs(med(f_in)), gbs(med(f_out))
     return {"value": min(off_gbs, pre_gbs), "unit": "GB/s",
+            "statistic": "median of the repetitions (each direction)",
             "h2d_bytes_per_step": 4 * N + link,
             "d2h_bytes_per_step": link + 8 * sum(segs) + 4 * N,
             "steps": reps, "offload_direction_gbs": off_gbs, "prefetch_direction_gbs": pre_gbs,
+            "best_gbs": min(gbs(min(t_in)), gbs(min(t_out))),
+            "mean_gbs": min(gbs(sum(t_in) / reps), gbs(sum(t_out) / reps)),
+            "offload_direction_ms": t_in, "prefetch_direction_ms": t_out,
             "compressed_link_bytes_per_direction": link,
             "link_floor": {"offload_direction_gbs": off_floor,
                            "prefetch_direction_gbs": pre_floor,
+                           "offload_direction_ms": f_in, "prefetch_direction_ms": f_out,
                            "frac_of_floor": min(off_gbs, pre_gbs) / min(off_floor, pre_floor),
                            "what": "plain pinned cudaMemcpyAsync of the same bytes, both ways "
-                                   "at once as in each direction of the step, no kernels; "
-                                   "uncompressed GB/s, best of the repetitions"},
+                                   "at once as in each direction of the step, no kernels, "
+                                   "right after each repetition; uncompressed GB/s, median"},
             "call": "H2D copy + zvc_offload per tensor, zvc_offload_join; zvc_prefetch + "
                     "D2H copy per tensor"}
 
