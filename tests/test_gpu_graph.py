@@ -138,3 +138,35 @@ def test_batched_compress_graph_replays_equal_the_oracle():
         S = int(size.item())
         assert S == ref.size and np.array_equal(out[:S].cpu().numpy(), ref), d
     assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+
+
+def test_compress16_graph_replays_equal_the_oracle():
+    ensure_lib()
+    rng = np.random.default_rng(10)
+    C, n = 1024, 1_000_003
+    x = torch.zeros(n, dtype=torch.int16, device="cuda")
+    cap = zvc.zvc_size_bound16(n, C)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    size = torch.zeros(1, dtype=torch.int64, device="cuda")
+    ws = zvc.new_workspace(zvc.zvc_workspace_size(n, C))
+
+    def comp(stream):
+        return zvc.zvc_compress16(x.data_ptr(), n, C, out.data_ptr(), cap, size.data_ptr(),
+                                  ws.data_ptr(), ws.numel(), stream)
+
+    assert comp(sh()) == zvc.ZVC_OK
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        assert comp(s.cuda_stream) == zvc.ZVC_OK
+    for d in (0.4, 0.02, 1.0):
+        w = rng.integers(1, 2**16, size=n, dtype=np.uint32).astype(np.uint16)
+        w[rng.random(n) >= d] = 0
+        x.copy_(torch.from_numpy(w.view(np.int16)).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.encode16(w, C)
+        S = int(size.item())
+        assert S == ref.size and np.array_equal(out[:S].cpu().numpy(), ref), d
+    assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
