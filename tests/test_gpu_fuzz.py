@@ -85,3 +85,37 @@ def test_random_case_equals_the_oracle(seed):
     assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
     for x, y in zip(xs, ys):
         assert torch.equal(x, y), (seed, T, C, ns)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_16bit_case_equals_the_oracle(seed):
+    """The same draws for the 16-bit calls (single streams)."""
+    ensure_lib()
+    rng = np.random.default_rng(5000 + seed)
+    C = int(rng.choice(CHUNKS))
+    n = int(np.exp(rng.uniform(0, np.log(300_000))))
+    w = rng.integers(1, 2**16, size=n, dtype=np.uint32).astype(np.uint16)
+    if rng.random() < 0.5:
+        w[rng.random(n) >= rng.random()] = 0
+    else:
+        blk = int(rng.choice([1, 7, 32, 100, 1024, 5000]))
+        keep = np.repeat(rng.random(n // blk + 1) < rng.random(), blk)[:n]
+        w[~keep] = 0
+    x = torch.from_numpy(w.view(np.int16)).cuda()
+    cap = zvc.zvc_size_bound16(n, C)
+    out = torch.full((cap + 64,), 0xEE, dtype=torch.uint8, device="cuda")
+    size = torch.zeros(1, dtype=torch.int64, device="cuda")
+    ws = zvc.new_workspace(zvc.zvc_workspace_size(n, C))
+    assert zvc.zvc_compress16(x.data_ptr(), n, C, out.data_ptr(), cap, size.data_ptr(),
+                              ws.data_ptr(), ws.numel(), sh()) == zvc.ZVC_OK
+    assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+    ref = oracle.encode16(w, C)
+    S = int(size.item())
+    host = out.cpu().numpy()
+    assert S == ref.size and np.array_equal(host[:S], ref), (seed, C, n)
+    assert (host[S:] == 0xEE).all()
+    y = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+    assert zvc.zvc_decompress16(out.data_ptr(), S, y.data_ptr(), n, C, ws.data_ptr(), ws.numel(),
+                                sh()) == zvc.ZVC_OK
+    assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+    assert torch.equal(x, y), (seed, C, n)
