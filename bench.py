@@ -76,6 +76,9 @@ def parse_args(argv=None):
     p.add_argument("--profile-density", type=float, default=None, metavar="D",
                    help="with --profile: a flat map of the same size with a fraction D of "
                         "i.i.d. non-zero words, instead of AlexNet layer 0")
+    p.add_argument("--profile-layer", type=int, default=0, metavar="L",
+                   help="with --profile compress|decompress: AlexNet layer L (0-4) of the "
+                        "batch-128 stack instead of layer 0")
     p.add_argument("--train", action="store_true",
                    help="training step of a VGG-style CNN with its saved activations kept, "
                         "offloaded compressed to host memory, or kept compressed in HBM; "
@@ -1001,7 +1004,9 @@ def run_profile_case(args):
         return run_profile_batch(args, torch, zvc, workloads)
     g = torch.Generator(device="cuda").manual_seed(1)
     c, h, w, d = workloads.ALEXNET_LAYERS[0]
-    if args.profile_density is None:
+    if args.profile_layer:
+        x = workloads.alexnet_stack(device="cuda")[args.profile_layer]
+    elif args.profile_density is None:
         b = torch.tensor(workloads.alexnet_biases(c, d, 1), device="cuda").view(1, c, 1, 1)
         x = torch.relu_(torch.randn((128, c, h, w), generator=g, device="cuda").add_(b))
     else:
@@ -1040,7 +1045,8 @@ def run_profile_case(args):
     if args.profile == "decompress":
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
     moved = 4 * n + S
-    print(json.dumps({"profile": args.profile, "density": args.profile_density, "n": n,
+    print(json.dumps({"profile": args.profile, "density": args.profile_density,
+                      "layer": args.profile_layer, "n": n,
                       "stream_bytes": S,
                       "ms": times[1:], "hbm_gbs": [moved / (t / 1e3) / 1e9 for t in times[1:]]}))
     return 0
