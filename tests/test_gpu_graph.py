@@ -170,3 +170,35 @@ def test_compress16_graph_replays_equal_the_oracle():
         S = int(size.item())
         assert S == ref.size and np.array_equal(out[:S].cpu().numpy(), ref), d
     assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+
+
+def test_static_compress_graph_replays_equal_the_oracle():
+    """zvc_compress_static captured and replayed: its epoch counter lives in the library's
+    static scratch, and every replay still equals the oracle."""
+    ensure_lib()
+    rng = np.random.default_rng(11)
+    C, n = 4096, 900_001
+    x = torch.zeros(n, dtype=torch.int32, device="cuda")
+    cap = zvc.zvc_size_bound(n, C)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    size = torch.zeros(1, dtype=torch.int64, device="cuda")
+
+    def comp(stream):
+        return zvc.zvc_compress_static(x.data_ptr(), n, C, out.data_ptr(), cap, size.data_ptr(),
+                                       stream)
+
+    assert comp(sh()) == zvc.ZVC_OK
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        assert comp(s.cuda_stream) == zvc.ZVC_OK
+    for d in (0.25, 0.75):
+        w = _words(rng, n, d)
+        x.copy_(torch.from_numpy(w.view(np.int32)).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.encode(w, C)
+        S = int(size.item())
+        assert S == ref.size and np.array_equal(out[:S].cpu().numpy(), ref), d
+    assert zvc.zvc_compress_static_get_error(sh()) == zvc.ZVC_OK
