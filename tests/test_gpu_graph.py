@@ -202,3 +202,72 @@ def test_static_compress_graph_replays_equal_the_oracle():
         S = int(size.item())
         assert S == ref.size and np.array_equal(out[:S].cpu().numpy(), ref), d
     assert zvc.zvc_compress_static_get_error(sh()) == zvc.ZVC_OK
+
+
+def test_batched_and_16bit_decompress_graph_replays_restore_the_input():
+    """Batched and 16-bit decompress captured and replayed on streams of new data of the same
+    size (the words moved within their windows): every replay restores its input."""
+    ensure_lib()
+    rng = np.random.default_rng(12)
+    C = 4096
+    ns = [300_017, 65_536, 1_000_000]
+    ws_ = [_words(rng, k, 0.35) for k in ns]
+    cap = zvc.zvc_batch_size_bound(ns, C)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    ws = zvc.new_workspace(zvc.ZVC_WORKSPACE_ALIGN)
+    ys = [torch.full((k,), -1, dtype=torch.int32, device="cuda") for k in ns]
+    ref = oracle.encode_batch(ws_, C)
+    out[:ref.size].copy_(torch.from_numpy(ref).cuda())
+    S = ref.size
+
+    def dec(stream):
+        return zvc.zvc_decompress_batched(out.data_ptr(), S, [y.data_ptr() for y in ys], ns, C,
+                                          ws.data_ptr(), ws.numel(), stream)
+
+    assert dec(sh()) == zvc.ZVC_OK
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        assert dec(s.cuda_stream) == zvc.ZVC_OK
+    for _ in range(3):
+        ws_ = [_permute_in_windows(rng, w) for w in ws_]
+        ref = oracle.encode_batch(ws_, C)
+        assert ref.size == S
+        out[:S].copy_(torch.from_numpy(ref).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        for w, y in zip(ws_, ys):
+            assert np.array_equal(y.cpu().numpy().view(np.uint32), w)
+    assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
+
+    # 16-bit: the same, one stream
+    n = 777_777
+    w16 = rng.integers(1, 2**16, size=n, dtype=np.uint32).astype(np.uint16)
+    w16[rng.random(n) >= 0.4] = 0
+    ref16 = oracle.encode16(w16, C)
+    S16 = ref16.size
+    out16 = torch.from_numpy(ref16).cuda()
+    y16 = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+
+    def dec16(stream):
+        return zvc.zvc_decompress16(out16.data_ptr(), S16, y16.data_ptr(), n, C, ws.data_ptr(),
+                                    ws.numel(), stream)
+
+    assert dec16(sh()) == zvc.ZVC_OK
+    torch.cuda.synchronize()
+    g16 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g16, stream=s):
+        assert dec16(s.cuda_stream) == zvc.ZVC_OK
+    for _ in range(3):
+        m = n - n % 32
+        v = w16[:m].reshape(-1, 32)
+        v = np.take_along_axis(v, np.argsort(rng.random(v.shape), axis=1), axis=1)
+        w16 = np.concatenate([v.reshape(-1), w16[m:]])
+        ref16 = oracle.encode16(w16, C)
+        assert ref16.size == S16
+        out16.copy_(torch.from_numpy(ref16).cuda())
+        g16.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(y16.cpu().numpy().view(np.uint16), w16)
+    assert zvc.zvc_get_error(ws.data_ptr(), sh()) == zvc.ZVC_OK
